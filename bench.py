@@ -1,0 +1,383 @@
+"""Benchmark: optimizer-step time per megabatch on one GB300 (or N replicas).
+
+One step = one Dion step (dion_step_batched, one call per shape group) over the
+whole megabatch of the workload.  The Newton-Schulz comparison path
+(muon_ns_batched over the same megabatch, per-head on attention QKV) is timed
+the same way and reported under "muon".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  Inputs are synthetic (workloads/), resident in
+HBM and larger than L2, so no L2 flush is needed between steps.  Timing: CUDA
+events on the launching stream, a barrier plus torch.cuda.synchronize() on both
+sides, max over ranks.  Per-kernel device times come from libdion's event
+recording around every launch inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step ms per megabatch; % of HBM (Dion) / bf16 tensor (NS) roofline"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------- clock sampling
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+                for k, name in enumerate(names):
+                    if r[5 + k].strip().lower().startswith("active"):
+                        reasons.add(name)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------- workload setup
+
+def build_state(w, device, seed0):
+    import workloads as wl
+    state = []
+    for gi, g in enumerate(w.groups):
+        r = g.rank(w.fraction)
+        X, M, Q = wl.make_state(g, r, w.dtype, device, seed0 + gi, w.x_std)
+        G = wl.make_grad(g, w.g_std, w.dtype, device, seed0 + gi, step=0)
+        state.append({"g": g, "r": r, "X": X, "M": M, "Q": Q, "G": G})
+    return state
+
+
+def dion_bytes_flops(g, r, dtype_bytes):
+    """Algorithmic traffic and flops of one Dion step on one shape group:
+    B read twice (M fp32 + G), M written once, X read and written, plus the
+    m x r and n x r panels; flops 8 m n r (B Q, B^T P, P R^T, P Q^T) plus
+    CholeskyQR2 (4 m r^2 + 2 m r^2 per pass)."""
+    mn = g.batch * g.m * g.n
+    by = mn * (2 * (4 + dtype_bytes) + 4 + 2 * dtype_bytes) + g.batch * 12 * (g.m + g.n) * r
+    fl = 8.0 * mn * r + g.batch * 12.0 * g.m * r * r
+    return by, fl
+
+
+def ns_flops(g, steps):
+    hd = g.head_dim if g.head_dim else g.n
+    heads = g.n // hd
+    s, l = min(g.m, hd), max(g.m, hd)
+    return g.batch * heads * steps * (4.0 * s * s * l + 2.0 * s ** 3)
+
+
+# per-kernel algorithmic bytes for the roofline of the dominant Dion kernel
+def kernel_bytes(name, w, state):
+    eb = 2 if str(w.dtype).endswith("bfloat16") else 4
+    tot = 0
+    for st in state:
+        g, r = st["g"], st["r"]
+        mn = g.batch * g.m * g.n
+        if name.startswith("dion_bq"):
+            tot += mn * (4 + eb) + g.batch * (g.n * r * 4 + g.m * r * 4)
+        elif name.startswith("dion_btp"):
+            tot += mn * (4 + eb) + g.batch * (g.m * r * 4 + g.n * r * 4)
+        elif name.startswith("dion_update"):
+            tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * r * 4 + 2 * g.n * r * 4)
+        elif name.startswith("dion_fused"):
+            tot += mn * (4 + eb + 4) + g.batch * (g.m * r * 4 + g.n * r * 4)
+        elif name.startswith("dion_xupd"):
+            tot += mn * (2 * eb) + g.batch * (g.m * r * 4 + g.n * r * 4)
+    return tot
+
+
+# ----------------------------------------------------------------- arms
+
+def run_gb300(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import orthonormal_optimizer_step_gb300 as od
+    import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]()
+    pk = peaks()
+    state = build_state(w, dev, 1000 + 17 * rank)
+    for st in state:
+        st["ws"] = od.new_workspace(od.dion_workspace_size(st["g"].batch, st["g"].m, st["g"].n, st["r"],
+                                                           od.DION_BF16 if st["X"].dtype == torch.bfloat16
+                                                           else od.DION_F32), dev)
+
+    def dion_step():
+        for st in state:
+            od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
+                                 workspace=st["ws"])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, steps, prof=None):
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if prof is not None:
+            prof.__enter__()
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        if prof is not None:
+            prof.__exit__(None, None, None)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                    if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+
+    # --- Dion (headline) ---
+    for _ in range(args.warmup):
+        dion_step()
+    clocks.start()
+    prof = od.profile(max_launches=64 * args.steps * len(state) + 64)
+    ms = timed(dion_step, args.steps, prof)
+    torch.cuda.synchronize()
+    kernels = prof.read()
+    gpu_launches = sum(v[0] for v in kernels.values())
+    ms_step = ms / args.steps
+    by, fl = 0, 0.0
+    eb = 2 if w.dtype == torch.bfloat16 else 4
+    for st in state:
+        b, f = dion_bytes_flops(st["g"], st["r"], eb)
+        by += b
+        fl += f
+    # dominant kernel by device time
+    dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else (None, (0, 0.0))
+    dom_name, (dom_launches, dom_ms) = dom
+    dom_bytes = kernel_bytes(dom_name or "", w, state) / max(1, len(state))
+    per_launch_ms = dom_ms / max(dom_launches, 1)
+    # every group launches the dominant kernel once per step: bytes per launch is the mean over groups
+    achieved = dom_bytes / (per_launch_ms * 1e-3) / 1e9 if dom_bytes and per_launch_ms > 0 else None
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": None,
+                "peak_source": pk["source"], "launches": dom_launches, "ms_per_launch": per_launch_ms,
+                "step_hbm_floor_ms": by / (pk["hbm_gbs"] * 1e9) * 1e3,
+                "step_tensor_floor_ms": fl / (pk["bf16_tflops"] * 1e12) * 1e3,
+                "step_frac_of_floor": max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)) * 1e3
+                / ms_step}
+
+    # --- Muon / Newton-Schulz comparison path ---
+    muon = None
+    if not args.skip_muon:
+        for st in state:
+            g = st["g"]
+            st["Mn"] = torch.zeros((g.batch, g.m, g.n), dtype=torch.float32, device=dev)
+            st["wsn"] = od.new_workspace(od.muon_workspace_size(g.batch, g.m, g.n, g.head_dim,
+                                                                od.DION_BF16 if w.dtype == torch.bfloat16
+                                                                else od.DION_F32), dev)
+
+        def muon_step():
+            for st in state:
+                od.muon_ns_batched(st["G"], X=st["X"], M=st["Mn"], head_dim=st["g"].head_dim, steps=w.ns_steps,
+                                   mu=w.mu, lr=w.lr, weight_decay=w.wd, workspace=st["wsn"])
+        msteps = max(1, args.steps // 2)
+        for _ in range(max(1, args.warmup)):
+            muon_step()
+        mprof = od.profile(max_launches=64 * msteps * len(state) * (w.ns_steps + 2))
+        mms = timed(muon_step, msteps, mprof) / msteps
+        mk = mprof.read()
+        nfl = sum(ns_flops(st["g"], w.ns_steps) for st in state)
+        gemm_ms = sum(v[1] for k, v in mk.items() if k.startswith("ns_") and ("gram" in k or "poly" in k
+                                                                              or "axpy" in k))
+        ach = nfl / (gemm_ms / msteps * 1e-3) / 1e12 if gemm_ms > 0 else None
+        muon = {"ms_per_step": mms, "tflops_step": nfl / (mms * 1e-3) / 1e12,
+                "roofline": {"bound": "tensor", "kernel": "ns gemm chain", "achieved": ach,
+                             "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,
+                             "peak_source": pk["source"]},
+                "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in mk.items()}}
+    clk = clocks.stop()
+
+    # --- end to end through the public API with host buffers ---
+    e2e = None
+    if not args.skip_e2e:
+        hostG = [st["G"].cpu().pin_memory() for st in state]
+        hostX = [torch.empty_like(st["X"], device="cpu").pin_memory() for st in state]
+        h2d = sum(t.numel() * t.element_size() for t in hostG)
+        d2h = sum(t.numel() * t.element_size() for t in hostX)
+
+        def e2e_step():
+            for st, hg, hx in zip(state, hostG, hostX):
+                st["G"].copy_(hg, non_blocking=True)
+                od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
+                                     workspace=st["ws"])
+                hx.copy_(st["X"], non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        esteps = max(1, args.steps // 2)
+        ems = timed(e2e_step, esteps) / esteps
+        e2e = {"value": ems / world, "unit": "ms", "ms_per_step": ems, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    # --- CPU baseline: the oracle on a bounded sample ---
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cpu = cpu_baseline(w, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": ms_step / world, "unit": "ms", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+                "data": "synthetic (seeded Gaussian, workloads/)",
+                "config": {"workload": w.name, "groups": [[g.batch, g.m, g.n, g.rank(w.fraction)]
+                                                          for g in w.groups],
+                           "rank_fraction": w.fraction, "params": w.params,
+                           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+                "clocks": clk, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
+                "muon": muon, "step_bytes": by, "step_flops": fl}
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, budget_s=20.0, seed=5):
+    """Times the oracle (as it stands) on one matrix per shape group for one
+    Dion step, and extrapolates to a megabatch step by the batch counts."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    total_ms = 0.0
+    sample = []
+    t_start = time.time()
+    for g in w.groups:
+        r = g.rank(w.fraction)
+        X = (0.02 * rng.standard_normal((g.m, g.n)))
+        G = w.g_std * rng.standard_normal((g.m, g.n))
+        M = np.zeros((g.m, g.n))
+        Q = rng.standard_normal((g.n, r))
+        Q /= np.linalg.norm(Q, axis=0)
+        t0 = time.perf_counter()
+        oracle.dion_step(X, G, M, Q, w.mu, w.lr, w.wd)
+        dt = (time.perf_counter() - t0) * 1e3
+        total_ms += dt * g.batch
+        sample.append(f"1x{g.m}x{g.n} r={r}")
+        if time.time() - t_start > budget_s:
+            return {"value": None, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
+                    "sample": "budget exceeded after " + ", ".join(sample)}
+    return {"value": total_ms, "unit": "ms", "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count())),
+            "kind": "oracle",
+            "sample": "one matrix per shape group (" + ", ".join(sample) + "), one Dion step each, "
+                      "scaled by the batch counts to one megabatch step"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle itself, on the host cores."""
+    if rank != 0:
+        return
+    import workloads as wl
+    w = wl.WORKLOADS[args.workload]()
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=1e9)
+    vals = []
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, budget_s=1e9)["value"])
+    ms = statistics.mean(vals)
+    cb = cpu_baseline(w, budget_s=1e9)
+    cb["value"] = ms
+    line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Gaussian)",
+            "config": {"workload": w.name}, "cpu_baseline": cb,
+            "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="gpt-small-megabatch")
+    ap.add_argument("--skip-muon", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "gb300" else args.warmup
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+// api.cu -- the C ABI of libdion: argument checks, workspace layout, dispatch.
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+
+namespace dion {
+
+static size_t carve(size_t& off, size_t bytes)
+{
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+}
+
+DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
+{
+    DionLayout L{};
+    L.tc = false;
+    L.rp = r;
+    L.ksplit = 1;
+    const size_t b = (size_t)batch, f = sizeof(float);
+    size_t off = 0;
+    L.status = carve(off, 256);
+    L.P0 = carve(off, b * m * L.rp * f);
+    L.P1 = carve(off, b * m * L.rp * f);
+    L.R = carve(off, b * n * L.rp * f);
+    L.S = carve(off, b * r * r * f);
+    L.W = carve(off, b * r * r * f);
+    L.dead = carve(off, b * r * sizeof(int));
+    L.inv = carve(off, b * L.rp * f);
+    L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Ps16 = L.nrm2 = off;
+    L.total = off;
+    (void)dt;
+    return L;
+}
+
+MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt)
+{
+    MuonLayout L{};
+    L.hd = head_dim > 0 ? head_dim : n;
+    L.heads = n / L.hd;
+    L.nb = batch * L.heads;
+    L.tr = m > L.hd;
+    L.s = std::min(m, L.hd);
+    L.l = std::max(m, L.hd);
+    L.tc = false;
+    const size_t nb = (size_t)L.nb, sl = (size_t)L.s * L.l, ss = (size_t)L.s * L.s, f = sizeof(float);
+    size_t off = 0;
+    L.status = carve(off, 256);
+    L.nrm = carve(off, nb * f);
+    L.Xa = carve(off, nb * sl * f);
+    L.Xb = carve(off, nb * sl * f);
+    L.XTa = L.XTb = off;
+    L.A = carve(off, nb * ss * f);
+    L.Bm = carve(off, nb * ss * f);
+    L.total = off;
+    (void)dt;
+    return L;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace dion
+
+using namespace dion;
+
+extern "C" const char* dion_status_string(dion_status s)
+{
+    switch (s) {
+    case DION_OK: return "ok";
+    case DION_ERR_INVALID_ARG: return "invalid argument";
+    case DION_ERR_UNSUPPORTED: return "unsupported";
+    case DION_ERR_WORKSPACE: return "workspace missing or too small";
+    case DION_ERR_CUDA: return "CUDA error";
+    case DION_ERR_NUMERIC: return "numeric breakdown on the device";
+    }
+    return "unknown status";
+}
+
+static bool dion_shape_ok(int batch, int m, int n, int r, dion_dtype dt)
+{
+    return batch >= 1 && batch <= 65535 && m >= 1 && n >= 1 && r >= 1 && r <= std::min(m, n) &&
+           (dt == DION_F32 || dt == DION_BF16);
+}
+
+extern "C" dion_status dion_workspace_size(int batch, int m, int n, int r, dion_dtype dt, size_t* bytes)
+{
+    if (!bytes || !dion_shape_ok(batch, m, n, r, dt)) return DION_ERR_INVALID_ARG;
+    *bytes = dion_layout(batch, m, n, r, dt).total;
+    return DION_OK;
+}
+
+extern "C" dion_status dion_workspace_panels(int batch, int m, int n, int r, dion_dtype dt, size_t* p_offset,
+                                             int* p_ld, size_t* r_offset, int* r_ld)
+{
+    if (!dion_shape_ok(batch, m, n, r, dt)) return DION_ERR_INVALID_ARG;
+    const DionLayout L = dion_layout(batch, m, n, r, dt);
+    if (p_offset) *p_offset = L.P0;
+    if (p_ld) *p_ld = L.rp;
+    if (r_offset) *r_offset = L.R;
+    if (r_ld) *r_ld = L.rp;
+    return DION_OK;
+}
+
+extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G,
+                                         float* M, float* Q, float mu, float lr, float weight_decay,
+                                         void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    if (!dion_shape_ok(batch, m, n, r, dt)) return DION_ERR_INVALID_ARG;
+    if (!X || !G || !M || !Q) return DION_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(G) || !aligned16(M) || !aligned16(Q)) return DION_ERR_INVALID_ARG;
+    if (!std::isfinite(mu) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return DION_ERR_INVALID_ARG;
+    const DionLayout L = dion_layout(batch, m, n, r, dt);
+    if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    return dion_step_simt(batch, m, n, r, dt, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);
+}
+
+static bool muon_shape_ok(int batch, int m, int n, int head_dim, dion_dtype dt)
+{
+    if (batch < 1 || m < 1 || n < 1 || head_dim < 0) return false;
+    if (head_dim > 0 && n % head_dim != 0) return false;
+    if (dt != DION_F32 && dt != DION_BF16) return false;
+    const long long nb = (long long)batch * (head_dim > 0 ? n / head_dim : 1);
+    return nb <= 65535;
+}
+
+extern "C" dion_status muon_workspace_size(int batch, int m, int n, int head_dim, dion_dtype dt, size_t* bytes)
+{
+    if (!bytes || !muon_shape_ok(batch, m, n, head_dim, dt)) return DION_ERR_INVALID_ARG;
+    *bytes = muon_layout(batch, m, n, head_dim, dt).total;
+    return DION_OK;
+}
+
+extern "C" dion_status muon_ns_batched(int batch, int m, int n, int head_dim, dion_dtype dt, void* X, const void* G,
+                                       float* M, void* O, int steps, const float* coeff, float mu, float lr,
+                                       float weight_decay, void* workspace, size_t workspace_bytes,
+                                       void* cuda_stream)
+{
+    if (!muon_shape_ok(batch, m, n, head_dim, dt)) return DION_ERR_INVALID_ARG;
+    if (!G || (!X && !O) || !coeff || steps < 0) return DION_ERR_INVALID_ARG;
+    if (!aligned16(G) || (X && !aligned16(X)) || (M && !aligned16(M)) || (O && !aligned16(O)))
+        return DION_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (!std::isfinite(coeff[i])) return DION_ERR_INVALID_ARG;
+    if (!std::isfinite(mu) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return DION_ERR_INVALID_ARG;
+    const MuonLayout L = muon_layout(batch, m, n, head_dim, dt);
+    if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    return muon_simt(batch, m, n, dt, X, G, M, O, steps, coeff, mu, lr, weight_decay, (char*)workspace, L, st);
+}
+
+extern "C" dion_status dion_get_status(const void* workspace, int* device_status)
+{
+    if (!workspace || !device_status) return DION_ERR_INVALID_ARG;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DION_ERR_CUDA;
+    *device_status = v;
+    return v ? DION_ERR_NUMERIC : DION_OK;
+}

@@ -1,0 +1,37 @@
+// internal.h -- host-side interfaces shared by libdion's translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace dion {
+
+// Workspace layout of dion_step_batched (byte offsets, each 256-aligned).
+struct DionLayout {
+    int rp;                 // r rounded up for the tensor-core path (== r on the fp32 path)
+    bool tc;                // tensor-core (bf16) path
+    int ksplit;             // split of the B Q contraction (partials in Ppart)
+    size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Ps16, nrm2, total;
+};
+DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
+
+// Workspace layout of muon_ns_batched.
+struct MuonLayout {
+    int heads, hd, s, l, nb;   // blocks per matrix, block width, Gram side, long side, total blocks
+    bool tr, tc;               // blocks transposed (m > hd); tensor-core path
+    size_t status, nrm, Xa, Xb, XTa, XTb, A, Bm, total;
+};
+MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt);
+
+// CholeskyQR2 of `batch` m x r float panels, in place in P (Ptmp is scratch of
+// the same size).  S, W: batch*r*r floats; dead: batch*r ints.
+cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,
+                         int* dead, int* status, cudaStream_t st);
+
+dion_status dion_step_simt(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
+                           float* Q, float mu, float lr, float wd, char* ws, const DionLayout& L,
+                           cudaStream_t st);
+dion_status muon_simt(int batch, int m, int n, dion_dtype dt, void* X, const void* G, float* M, void* O,
+                      int steps, const float* coeff, float mu, float lr, float wd, char* ws,
+                      const MuonLayout& L, cudaStream_t st);
+
+}  // namespace dion

@@ -1,0 +1,155 @@
+"""GPU parity of dion_step_batched against the oracle (teacher-forced: both
+sides start every step from the same stored state).  Calls go through the C
+ABI (ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+import orthonormal_optimizer_step_gb300 as od
+from parity import ORTH_TOL, TOL, dion_pair, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _check(out, dtype, x_rel=True):
+    tol = TOL[dtype]
+    assert out["orth"] <= ORTH_TOL, out
+    for key in ("M", "Q", "R", "PQt"):
+        assert out[key] <= tol, (key, out)
+    if x_rel:
+        assert out["X"] <= tol, ("X", out)
+    if dtype == torch.bfloat16:
+        assert out["x_ulps"] <= 1.0 + 1e-9, out
+
+
+def test_single_256_fp32_ten_steps():
+    """256 x 256 float32, rank 64, mu = 0.95, lr = wd = 0.01, ten steps with a
+    fresh N(0, 1) gradient each step; every step is compared."""
+    w = wl.single_256()
+    g = w.groups[0]
+    r = g.rank(w.fraction)
+    assert r == 64
+    X, M, Q = wl.make_state(g, r, w.dtype, DEV, seed=1001)
+    for step in range(w.steps):
+        G = wl.make_grad(g, w.g_std, w.dtype, DEV, seed=1001, step=step)
+        out = dion_pair(X, G, M, Q, w.mu, w.lr, w.wd)
+        assert out["status"] == 0
+        _check(out, w.dtype)
+
+
+RAGGED = [
+    (3, 200, 136, 24, torch.float32),
+    (2, 136, 200, 136, torch.float32),     # r = m = min(m, n)
+    (2, 200, 136, 136, torch.bfloat16),    # r = n = min(m, n)
+    (1, 97, 131, 1, torch.float32),        # r = 1, odd sizes
+    (2, 130, 260, 17, torch.bfloat16),
+    (1, 64, 64, 64, torch.bfloat16),
+    (1, 8, 520, 3, torch.bfloat16),        # very wide
+    (2, 520, 8, 8, torch.float32),         # very tall, full rank
+]
+
+
+@pytest.mark.parametrize("batch,m,n,r,dtype", RAGGED)
+def test_ragged_shapes(batch, m, n, r, dtype):
+    g = wl.Group(batch, m, n)
+    seed = 7 + m + n + r
+    X, _, Q = wl.make_state(g, r, dtype, DEV, seed)
+    M = wl.make_momentum(g, 0.5, DEV, seed)
+    G = wl.make_grad(g, 1.0, dtype, DEV, seed, step=3)
+    # lr = 0.5 makes the weight change span many bf16 units, so its direction is checked too
+    out = dion_pair(X, G, M, Q, 0.9, 0.5, 0.02)
+    assert out["status"] == 0
+    _check(out, dtype)
+
+
+def test_gpt_small_megabatch_sampled():
+    """Full GPT-small megabatch (12 matrices per shape group), bf16, rank 192;
+    the oracle checks one sampled matrix of every group (matrices of a batch
+    are independent)."""
+    w = wl.gpt_small()
+    for gi, g in enumerate(w.groups):
+        r = g.rank(w.fraction)
+        X, _, Q = wl.make_state(g, r, w.dtype, DEV, seed=2000 + gi)
+        M = wl.make_momentum(g, w.g_std, DEV, seed=2000 + gi)
+        G = wl.make_grad(g, w.g_std, w.dtype, DEV, seed=2000 + gi, step=1)
+        out = dion_pair(X, G, M, Q, w.mu, w.lr, w.wd, samples=[5])
+        assert out["status"] == 0
+        _check(out, w.dtype, x_rel=False)
+
+
+def test_zero_gradient_reports_breakdown_and_stays_finite():
+    g = wl.Group(2, 64, 96)
+    X, M, Q = wl.make_state(g, 8, torch.bfloat16, DEV, seed=5)
+    G = torch.zeros_like(X)
+    X0 = X.clone()
+    ws = od.dion_step_batched(X, G, M, Q, mu=0.95, lr=0.01, weight_decay=0.1)
+    torch.cuda.synchronize()
+    st = od.dion_get_status(ws)
+    assert st & 1
+    assert torch.isfinite(Q).all() and torch.isfinite(M).all() and torch.isfinite(X.float()).all()
+    assert torch.count_nonzero(M) == 0
+    # B = 0: only the decay acts on X (computed in float32 as the kernel does)
+    decay = np.float32(1.0) - np.float32(0.01) * np.float32(0.1)
+    ref = (X0.float() * float(decay)).to(torch.bfloat16)
+    assert torch.equal(X, ref)
+
+
+def test_rank_deficient_gradient():
+    """G of rank 2 with r = 6: dependent columns of P are zeroed and flagged;
+    the rest stay orthonormal."""
+    g = wl.Group(1, 48, 40)
+    gen = torch.Generator(device="cpu").manual_seed(3)
+    u = torch.randn(48, 2, generator=gen, dtype=torch.float64)
+    v = torch.randn(2, 40, generator=gen, dtype=torch.float64)
+    G = (u @ v).to(torch.float32).unsqueeze(0).to(DEV)
+    X, M, Q = wl.make_state(g, 6, torch.float32, DEV, seed=9)
+    ws = od.dion_step_batched(X, G, M, Q, mu=0.9, lr=0.01, weight_decay=0.0)
+    torch.cuda.synchronize()
+    assert od.dion_get_status(ws) & 1
+    P, _ = od.dion_panels(ws, 1, 48, 40, 6, od.DION_F32)
+    P = f64(P[0])
+    live = np.linalg.norm(P, axis=0) > 0.5
+    assert 1 <= live.sum() <= 2 + 1
+    np.testing.assert_allclose(P[:, live].T @ P[:, live], np.eye(live.sum()), atol=1e-3)
+    assert np.all(np.abs(P[:, ~live]) == 0)
+    assert torch.isfinite(X).all() and torch.isfinite(M).all() and torch.isfinite(Q).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_checkpoint_resume_is_bitwise(dtype):
+    """The optimizer state is (X, M, Q): saving it, reloading it and stepping
+    gives exactly the uninterrupted run."""
+    g = wl.Group(3, 192, 320)
+    r = 48
+    X, M, Q = wl.make_state(g, r, dtype, DEV, seed=77)
+    grads = [wl.make_grad(g, 1.0, dtype, DEV, 77, s) for s in range(5)]
+    for s in range(3):
+        od.dion_step_batched(X, grads[s], M, Q, mu=0.9, lr=0.02, weight_decay=0.01)
+    saved = [t.clone() for t in (X, M, Q)]
+    for s in range(3, 5):
+        od.dion_step_batched(X, grads[s], M, Q, mu=0.9, lr=0.02, weight_decay=0.01)
+    X2, M2, Q2 = [t.clone() for t in saved]
+    for s in range(3, 5):
+        od.dion_step_batched(X2, grads[s], M2, Q2, mu=0.9, lr=0.02, weight_decay=0.01)
+    torch.cuda.synchronize()
+    assert torch.equal(X, X2) and torch.equal(M, M2) and torch.equal(Q, Q2)
+
+
+def test_streams_and_reused_workspace():
+    """A caller stream and a reused workspace give the same result as the
+    default stream with a fresh one."""
+    g = wl.Group(2, 128, 256)
+    X, M, Q = wl.make_state(g, 32, torch.bfloat16, DEV, seed=4)
+    G = wl.make_grad(g, 1.0, torch.bfloat16, DEV, 4, 0)
+    A = [t.clone() for t in (X, M, Q)]
+    od.dion_step_batched(*A[:1], G, *A[1:], mu=0.9, lr=0.1, weight_decay=0.0)
+    s = torch.cuda.Stream()
+    ws = od.new_workspace(od.dion_workspace_size(2, 128, 256, 32, od.DION_BF16), DEV)
+    ws.fill_(0xAB)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        od.dion_step_batched(X, G, M, Q, mu=0.9, lr=0.1, weight_decay=0.0, workspace=ws, stream=s)
+    s.synchronize()
+    assert torch.equal(X, A[0]) and torch.equal(M, A[1]) and torch.equal(Q, A[2])
