@@ -63,11 +63,11 @@ def dion_pair(X, G, M, Q, mu, lr, wd, samples=None):
         out["X"] = max(out["X"], rel(dX_g, dX_o))
         if dt == torch.bfloat16:
             # X itself: within one bf16 unit in the last place of the larger of
-            # the two roundings, plus the float32 error of the unrounded value
-            # (which decides the rounding where X' is near zero).
+            # the two roundings, plus the tolerated error of the update itself
+            # (which decides the rounding where X' is near a rounding boundary).
             mag = np.maximum(np.maximum(np.abs(Xo), np.abs(Xg)), 1e-30)
             ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
-            slack = 2e-3 * TOL[dt] * (np.abs(host["X"][k]) + np.abs(dX_o)).max()
+            slack = TOL[dt] * np.abs(o["X"] - host["X"][k]).max()
             out["x_ulps"] = max(out["x_ulps"], float(np.max(np.abs(Xg - Xo) / (ulp + slack))))
     out["status"] = status
     return out
