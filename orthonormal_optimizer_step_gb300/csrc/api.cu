@@ -13,25 +13,48 @@ static size_t carve(size_t& off, size_t bytes)
     return at;
 }
 
+// Splits of a streaming contraction so that one wave of CTAs covers the SMs
+// (one CTA per SM); fixed per shape so that the workspace size is too.
+static int stream_splits(long long base_ctas, int kchunks)
+{
+    const int sms = 152;
+    int s = (int)((sms + base_ctas / 2) / base_ctas);
+    if (s < 1) s = 1;
+    if (s > kchunks) s = kchunks;
+    const int per = (kchunks + s - 1) / s;
+    return (kchunks + per - 1) / per;
+}
+
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
 {
     DionLayout L{};
-    L.tc = false;
-    L.rp = r;
-    L.ksplit = 1;
-    const size_t b = (size_t)batch, f = sizeof(float);
+    L.tc = (dt == DION_BF16);
+    L.rp = L.tc ? (int)align_up((size_t)r, 64) : r;   // MN-major operand blocks are 64 wide
+    const size_t b = (size_t)batch, f = sizeof(float), h = 2, rp = (size_t)L.rp;
+    L.ksplit = L.ksplit_r = 1;
     size_t off = 0;
     L.status = carve(off, 256);
-    L.P0 = carve(off, b * m * L.rp * f);
-    L.P1 = carve(off, b * m * L.rp * f);
-    L.R = carve(off, b * n * L.rp * f);
+    L.P0 = carve(off, b * m * rp * f);
+    L.P1 = carve(off, b * m * rp * f);
+    L.R = carve(off, b * n * rp * f);
     L.S = carve(off, b * r * r * f);
     L.W = carve(off, b * r * r * f);
     L.dead = carve(off, b * r * sizeof(int));
-    L.inv = carve(off, b * L.rp * f);
-    L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Ps16 = L.nrm2 = off;
+    L.inv = carve(off, b * rp * f);
+    if (L.tc) {
+        const int rch = (int)cdiv(L.rp, 256);
+        L.ksplit = stream_splits(cdiv(m, 128) * rch * batch, (int)cdiv(n, 64));
+        L.ksplit_r = stream_splits(cdiv(n, 128) * rch * batch, (int)cdiv(m, 64));
+        const size_t rows = std::max((size_t)L.ksplit * m, (size_t)L.ksplit_r * n);
+        L.Ppart = carve(off, rows * b * rp * f);
+        L.Qt16 = carve(off, b * rp * align_up((size_t)n, 8) * h);
+        L.P16 = carve(off, b * m * rp * h);
+        L.R16 = carve(off, b * n * rp * h);
+        L.Q16 = carve(off, b * n * rp * h);
+    } else {
+        L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
+    }
     L.total = off;
-    (void)dt;
     return L;
 }
 
@@ -44,18 +67,32 @@ MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt)
     L.tr = m > L.hd;
     L.s = std::min(m, L.hd);
     L.l = std::max(m, L.hd);
-    L.tc = false;
-    const size_t nb = (size_t)L.nb, sl = (size_t)L.s * L.l, ss = (size_t)L.s * L.s, f = sizeof(float);
+    L.tc = (dt == DION_BF16);
+    const size_t nb = (size_t)L.nb, f = sizeof(float);
     size_t off = 0;
     L.status = carve(off, 256);
     L.nrm = carve(off, nb * f);
-    L.Xa = carve(off, nb * sl * f);
-    L.Xb = carve(off, nb * sl * f);
-    L.XTa = L.XTb = off;
-    L.A = carve(off, nb * ss * f);
-    L.Bm = carve(off, nb * ss * f);
+    if (L.tc) {
+        L.lp = (int)align_up((size_t)L.l, 8);
+        L.sp = (int)align_up((size_t)L.s, 8);
+        const size_t h = sizeof(uint16_t);
+        L.Xa = carve(off, nb * L.s * L.lp * h);
+        L.Xb = carve(off, nb * L.s * L.lp * h);
+        L.XTa = carve(off, nb * L.l * L.sp * h);
+        L.XTb = carve(off, nb * L.l * L.sp * h);
+        L.A = carve(off, nb * L.s * L.sp * h);
+        L.Bm = carve(off, nb * L.s * L.sp * h);
+    } else {
+        L.lp = L.l;
+        L.sp = L.s;
+        const size_t sl = (size_t)L.s * L.l, ss = (size_t)L.s * L.s;
+        L.Xa = carve(off, nb * sl * f);
+        L.Xb = carve(off, nb * sl * f);
+        L.XTa = L.XTb = off;
+        L.A = carve(off, nb * ss * f);
+        L.Bm = carve(off, nb * ss * f);
+    }
     L.total = off;
-    (void)dt;
     return L;
 }
 
@@ -114,6 +151,7 @@ extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dt
     const DionLayout L = dion_layout(batch, m, n, r, dt);
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)cuda_stream;
+    if (L.tc) return dion_step_tc(batch, m, n, r, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);
     return dion_step_simt(batch, m, n, r, dt, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);
 }
 
@@ -148,6 +186,8 @@ extern "C" dion_status muon_ns_batched(int batch, int m, int n, int head_dim, di
     const MuonLayout L = muon_layout(batch, m, n, head_dim, dt);
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)cuda_stream;
+    if (L.tc)
+        return muon_tc(batch, m, n, dt, X, G, M, O, steps, coeff, mu, lr, weight_decay, (char*)workspace, L, st);
     return muon_simt(batch, m, n, dt, X, G, M, O, steps, coeff, mu, lr, weight_decay, (char*)workspace, L, st);
 }
 

@@ -1,0 +1,554 @@
+// dion_tc.cu -- the Dion step on the tensor cores, for bf16 weights/gradients.
+//
+// Per megabatch of m x n matrices at rank r (rp = r rounded up to 64, the
+// width of one 128-byte swizzle block of bf16):
+//   1. dion_prep_qt  : Qt = bf16(Q^T)                      (rp x n, K-major operand)
+//   2. dion_bq_tc    : P = B Q with B = M + G formed in registers, rounded to
+//                      bf16 and written straight into the swizzled MMA operand
+//                      tile (B is never stored); split over n, fp32 partials
+//   3. dion_reduce   : P = sum of partials
+//   4. CholeskyQR2 of P (float32)
+//   5. dion_prep_p   : P16 = bf16(P)
+//   6. dion_btp_tc   : R = B^T P, contracting over m: both operands are read
+//                      MN-major (B rows are K rows), so B is again formed in
+//                      registers without any transpose; split over m
+//   7. dion_reduce   : R = sum of partials; column norms; Q = R / ||R_j||
+//   8. dion_prep_rq  : R16 = bf16(R), Q16 = bf16(Q)
+//   9. dion_update_tc: per 128 x 64 tile, two accumulators P R^T and P Q^T in
+//                      tensor memory; the epilogue streams M, G, X once:
+//                      M <- M + G - (1-mu) P R^T,  X <- (1-lr wd) X - lr sqrt(m/n) P Q^T
+// The MMAs are tcgen05.mma kind::f16 (bf16 in, fp32 accumulate); tiles reach
+// shared memory by TMA (Q, P, R operands) or from the producer warps (B).
+#include "internal.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace dion {
+
+int num_sms();
+
+namespace {
+
+constexpr int kBM = 128, kBK = 64;
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8])
+{
+    uint4 u;
+    u.x = tc::pack_bf16x2(v[0], v[1]);
+    u.y = tc::pack_bf16x2(v[2], v[3]);
+    u.z = tc::pack_bf16x2(v[4], v[5]);
+    u.w = tc::pack_bf16x2(v[6], v[7]);
+    return u;
+}
+
+// v[0..8) = M[o..o+8) + G[o..o+8) for columns col..col+7 of row i; zero outside
+// the matrix.  VEC: 16-byte vector loads (needs n % 8 == 0).
+template <bool VEC>
+__device__ __forceinline__ void load_b8(const float* M, const bf16* G, long long rowbase, int i, int m, int col, int n,
+                                        float (&v)[8])
+{
+    if (VEC && i < m && col + 8 <= n) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(M + rowbase + col));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(M + rowbase + col + 4));
+        const uint4 g = __ldg(reinterpret_cast<const uint4*>(G + rowbase + col));
+        const bf16* h = reinterpret_cast<const bf16*>(&g);
+        v[0] = a.x + __bfloat162float(h[0]); v[1] = a.y + __bfloat162float(h[1]);
+        v[2] = a.z + __bfloat162float(h[2]); v[3] = a.w + __bfloat162float(h[3]);
+        v[4] = c.x + __bfloat162float(h[4]); v[5] = c.y + __bfloat162float(h[5]);
+        v[6] = c.z + __bfloat162float(h[6]); v[7] = c.w + __bfloat162float(h[7]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = col + e;
+            v[e] = (i < m && c < n) ? M[rowbase + c] + __bfloat162float(G[rowbase + c]) : 0.f;
+        }
+    }
+}
+
+struct PassArgs {
+    int m, n, rp, batch;
+    int rchunks;            // r-chunks of 256 columns
+    int kchunks_per_split;  // 64-wide K chunks per split
+    int kchunks;            // total K chunks
+    const float* M;
+    const bf16* G;
+    float* part;            // [split][batch][rows][rp] fp32 partial products
+    int* status;
+};
+
+constexpr int kProducers = 256;   // 8 producer warps; warp 8 issues the MMAs
+constexpr int kStages = 4;
+constexpr uint32_t kAB = kBM * kBK * 2;          // 16 KB bf16 A tile
+constexpr uint32_t kBB = 256 * kBK * 2;          // up to 32 KB B tile
+constexpr uint32_t kStage = kAB + kBB;
+constexpr size_t kPassSmem = (size_t)kStages * kStage + 1024 + 256;
+
+// Shared skeleton of the two streaming passes.  MN_A = false: pass 2 (P = B Q),
+// A tile = 128 rows of B x 64 columns, K-major.  MN_A = true: pass 6
+// (R = B^T P), A tile = 64 rows of B x 128 columns, MN-major.
+template <bool MN_A, bool VEC>
+__global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB, PassArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + kStages * kStage);
+    uint64_t* empty = full + kStages;
+    uint64_t* done = empty + kStages;
+    uint32_t* tmem_slot = (uint32_t*)(done + 1);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    volatile int* abrt = abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int tile = blockIdx.x;                       // 128-wide output row tile
+    const int rc = blockIdx.y % a.rchunks, split = blockIdx.y / a.rchunks;
+    const int b = blockIdx.z;
+    const int nN = min(256, a.rp - rc * 256);          // MMA N (multiple of 64)
+    const int nbox = min(256, a.rp);                   // rows (or columns) of one B box
+    const int kc0 = split * a.kchunks_per_split;
+    const int nk = min(a.kchunks_per_split, a.kchunks - kc0);
+    const int out_rows = MN_A ? a.n : a.m;
+    const uint32_t b_bytes = MN_A ? (uint32_t)((nbox + 63) / 64) * 8192u : (uint32_t)nbox * 128u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&full[s], kProducers + 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 8) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 8) {
+        // ---------------- producers: B = M + G -> bf16 -> swizzled A tile
+        for (int kc = 0; kc < nk && !*abrt; ++kc) {
+            const int stage = kc % kStages;
+            const uint32_t ph = (kc / kStages) & 1;
+            if (lane == 0) tc::mbar_wait(&empty[stage], ph ^ 1, abrt, a.status);
+            __syncwarp();
+            if (*abrt) break;
+            uint8_t* sA = smem + stage * kStage;
+            const int k0 = (kc0 + kc) * kBK;
+            if (threadIdx.x == 0) {
+                tc::mbar_arrive_expect_tx(&full[stage], b_bytes);
+                if (MN_A) {
+                    for (int blk = 0; blk * 64 < nbox; ++blk)
+                        tc::tma_load_3d(sA + kAB + blk * 8192, &tmB, &full[stage], rc * 256 + blk * 64, k0, b);
+                } else {
+                    tc::tma_load_3d(sA + kAB, &tmB, &full[stage], k0, rc * 256, b);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = threadIdx.x + kProducers * u;
+                float v[8];
+                uint32_t off;
+                if (!MN_A) {
+                    const int row = g >> 3, ch = g & 7;             // 128 rows x 8 chunks
+                    const int i = tile * kBM + row;
+                    load_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, k0 + ch * 8, a.n, v);
+                    off = tc::sw128_offset(row, ch);
+                } else {
+                    const int row = g >> 4, ch = g & 15;            // 64 K-rows x 16 chunks
+                    const int i = k0 + row;
+                    load_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, tile * kBM + ch * 8, a.n, v);
+                    off = (ch >> 3) * 8192u + tc::sw128_offset(row, ch & 7);
+                }
+                *reinterpret_cast<uint4*>(sA + off) = pack8(v);
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&full[stage]);
+        }
+    } else if (lane == 0) {
+        // ---------------- MMA issuer
+        const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, MN_A);
+        for (int kc = 0; kc < nk; ++kc) {
+            const int stage = kc % kStages;
+            const uint32_t ph = (kc / kStages) & 1;
+            if (!tc::mbar_wait(&full[stage], ph, abrt, a.status)) break;
+            tc::tc_fence_after();
+            const uint32_t a0 = tc::smem_u32(smem + stage * kStage), b0 = a0 + kAB;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+                uint64_t ad, bd;
+                if (MN_A) {
+                    ad = tc::make_sdesc(a0 + k * 2048, 8192, 1024);
+                    bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
+                } else {
+                    ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
+                    bd = tc::make_sdesc(b0 + k * 32, 16, 1024);
+                }
+                tc::mma_bf16(tmem, ad, bd, idesc, (kc | k) != 0);
+            }
+            tc::mma_commit(&empty[stage]);
+        }
+        tc::mma_commit(done);
+    }
+
+    if (warp < 4) {
+        // ---------------- epilogue: TMEM -> fp32 partials
+        const bool ok = tc::mbar_wait(done, 0, abrt, a.status);
+        tc::tc_fence_after();
+        const int row = tile * kBM + warp * 32 + lane;
+        float* out = a.part + (((long long)split * a.batch + b) * out_rows + row) * a.rp + rc * 256;
+        for (int c0 = 0; c0 < nN; c0 += 32) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tc::tmem_ld_wait();
+            if (ok && row < out_rows) {
+                const int nv = min(32, nN - c0);
+                for (int j = 0; j < nv; j += 4)
+                    *reinterpret_cast<float4*>(out + c0 + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
+            }
+        }
+        tc::tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 8) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
+// ------------------------------------------------------------ the update pass
+struct UpdArgs {
+    int m, n, rp, kchunks;
+    float* M;
+    const bf16* G;
+    bf16* X;
+    float one_minus_mu, decay, scale;
+    int* status;
+};
+
+constexpr int kUBN = 64, kUStages = 3;
+constexpr uint32_t kUA = kBM * kBK * 2, kUB = kUBN * kBK * 2, kUStage = kUA + 2 * kUB;
+constexpr size_t kUpdSmem = (size_t)kUStages * kUStage + 1024 + 256;
+
+template <bool VEC>
+__global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_constant__ CUtensorMap tmP,
+                                                             const __grid_constant__ CUtensorMap tmR,
+                                                             const __grid_constant__ CUtensorMap tmQ, UpdArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + kUStages * kUStage);
+    uint64_t* empty = full + kUStages;
+    uint64_t* done = empty + kUStages;
+    uint32_t* tmem_slot = (uint32_t*)(done + 1);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    volatile int* abrt = abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, mt = blockIdx.y, b = blockIdx.z;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kUStages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 128);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            for (int kc = 0; kc < a.kchunks; ++kc) {
+                const int stage = kc % kUStages;
+                const uint32_t ph = (kc / kUStages) & 1;
+                if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, a.status)) break;
+                uint8_t* s = smem + stage * kUStage;
+                tc::mbar_arrive_expect_tx(&full[stage], kUStage);
+                tc::tma_load_3d(s, &tmP, &full[stage], kc * kBK, mt * kBM, b);
+                tc::tma_load_3d(s + kUA, &tmR, &full[stage], kc * kBK, nt * kUBN, b);
+                tc::tma_load_3d(s + kUA + kUB, &tmQ, &full[stage], kc * kBK, nt * kUBN, b);
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::make_idesc(kBM, kUBN, 1, false, false);
+            for (int kc = 0; kc < a.kchunks; ++kc) {
+                const int stage = kc % kUStages;
+                const uint32_t ph = (kc / kUStages) & 1;
+                if (!tc::mbar_wait(&full[stage], ph, abrt, a.status)) break;
+                tc::tc_fence_after();
+                const uint32_t a0 = tc::smem_u32(smem + stage * kUStage), r0 = a0 + kUA, q0 = r0 + kUB;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k) {
+                    const uint64_t ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
+                    tc::mma_bf16(tmem, ad, tc::make_sdesc(r0 + k * 32, 16, 1024), idesc, (kc | k) != 0);
+                    tc::mma_bf16(tmem + kUBN, ad, tc::make_sdesc(q0 + k * 32, 16, 1024), idesc, (kc | k) != 0);
+                }
+                tc::mma_commit(&empty[stage]);
+            }
+            tc::mma_commit(done);
+        }
+    } else {
+        // epilogue warps 0..3: row = one TMEM lane
+        const int i = mt * kBM + warp * 32 + lane;
+        const bool ok = tc::mbar_wait(done, 0, abrt, a.status);
+        tc::tc_fence_after();
+        for (int c0 = 0; c0 < kUBN; c0 += 32) {
+            uint32_t pr[32], pq[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, pr);
+            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(kUBN + c0), pq);
+            tc::tmem_ld_wait();
+            const int j0 = nt * kUBN + c0;
+            if (!ok || i >= a.m || j0 >= a.n) continue;
+            const long long o = ((long long)b * a.m + i) * a.n + j0;
+            if (VEC && j0 + 32 <= a.n) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float4 m0 = *reinterpret_cast<const float4*>(a.M + o + 8 * q);
+                    float4 m1 = *reinterpret_cast<const float4*>(a.M + o + 8 * q + 4);
+                    const uint4 g = __ldg(reinterpret_cast<const uint4*>(a.G + o + 8 * q));
+                    const uint4 x = *reinterpret_cast<const uint4*>(a.X + o + 8 * q);
+                    const bf16* gh = reinterpret_cast<const bf16*>(&g);
+                    const bf16* xh = reinterpret_cast<const bf16*>(&x);
+                    float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                    float xv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        mv[e] = mv[e] + __bfloat162float(gh[e]) - a.one_minus_mu * __uint_as_float(pr[8 * q + e]);
+                        xv[e] = a.decay * __bfloat162float(xh[e]) - a.scale * __uint_as_float(pq[8 * q + e]);
+                    }
+                    *reinterpret_cast<float4*>(a.M + o + 8 * q) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+                    *reinterpret_cast<float4*>(a.M + o + 8 * q + 4) = make_float4(mv[4], mv[5], mv[6], mv[7]);
+                    *reinterpret_cast<uint4*>(a.X + o + 8 * q) = pack8(xv);
+                }
+            } else {
+                const int nv = min(32, a.n - j0);
+                for (int e = 0; e < nv; ++e) {
+                    a.M[o + e] = a.M[o + e] + __bfloat162float(a.G[o + e]) - a.one_minus_mu * __uint_as_float(pr[e]);
+                    a.X[o + e] = __float2bfloat16_rn(a.decay * __bfloat162float(a.X[o + e]) -
+                                                     a.scale * __uint_as_float(pq[e]));
+                }
+            }
+        }
+        tc::tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 128);
+    }
+}
+
+// ------------------------------------------------------------ small kernels
+
+// Qt[b][j][k] = bf16(Q[b][k][j]) for j < r; zero rows r <= j < rp.
+__global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp, long long ldqt, const float* Q,
+                                                           bf16* Qt)
+{
+    __shared__ float tile[32][33];
+    const int b = blockIdx.z, k0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+    for (int kk = threadIdx.y; kk < 32; kk += 8) {
+        const int k = k0 + kk, j = j0 + threadIdx.x;
+        tile[kk][threadIdx.x] = (k < n && j < r) ? Q[((long long)b * n + k) * r + j] : 0.f;
+    }
+    __syncthreads();
+    for (int jj = threadIdx.y; jj < 32; jj += 8) {
+        const int j = j0 + jj, k = k0 + threadIdx.x;
+        if (j < rp && k < n) Qt[((long long)b * rp + j) * ldqt + k] = __float2bfloat16_rn(tile[threadIdx.x][jj]);
+    }
+}
+
+// dst[e] = sum_s part[s][e] over `count` floats (count % 4 == 0).
+__global__ void __launch_bounds__(256) dion_reduce_kernel(long long count, int splits, const float* part, float* dst)
+{
+    const long long n4 = count / 4;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += (long long)gridDim.x * blockDim.x) {
+        float4 s = reinterpret_cast<const float4*>(part)[e];
+        for (int k = 1; k < splits; ++k) {
+            const float4 t = reinterpret_cast<const float4*>(part + (long long)k * count)[e];
+            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+        }
+        reinterpret_cast<float4*>(dst)[e] = s;
+    }
+}
+
+// dst = bf16(src) over rows x rp, with columns c >= r set to zero.  If inv is
+// given, column c is scaled by inv[b*r + c] (Q16 = bf16(R / ||R_c||)).
+__global__ void __launch_bounds__(256) dion_to_bf16_kernel(long long rows_total, int rows, int r, int rp,
+                                                           const float* src, const float* inv, bf16* dst)
+{
+    const long long total = rows_total * rp;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % rp);
+        const long long row = e / rp;
+        float v = 0.f;
+        if (c < r) {
+            v = src[e];
+            if (inv) v *= inv[(row / rows) * r + c];
+        }
+        dst[e] = __float2bfloat16_rn(v);
+    }
+}
+
+}  // namespace
+
+// Q_j <- R_j / max(||R_j||, floor) over the n rows of R (pitch ldr >= r).
+__global__ void __launch_bounds__(256) dion_colnorm_tc_kernel(int n, int r, long long ldr, const float* R, float* Q,
+                                                              float* inv_out, float floor_nrm, int* status)
+{
+    __shared__ float red[8][33];
+    __shared__ float s_inv[32];
+    const int b = blockIdx.y, tx = threadIdx.x, ty = threadIdx.y;
+    const int j = blockIdx.x * 32 + tx;
+    const float* Rb = R + (size_t)b * n * ldr;
+    float s = 0.f;
+    if (j < r)
+        for (int i = ty; i < n; i += 8) {
+            const float v = Rb[(size_t)i * ldr + j];
+            s = fmaf(v, v, s);
+        }
+    red[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0) {
+        float t = 0.f;
+        for (int k = 0; k < 8; ++k) t += red[k][tx];
+        const float inv = 1.f / fmaxf(sqrtf(t), floor_nrm);
+        s_inv[tx] = inv;
+        if (j < r) {
+            inv_out[(size_t)b * r + j] = inv;
+            if (!isfinite(t)) atomicOr(status, kStatusNonFinite);
+        }
+    }
+    __syncthreads();
+    if (j < r) {
+        float* Qb = Q + (size_t)b * n * r;
+        for (int i = ty; i < n; i += 8) Qb[(size_t)i * r + j] = Rb[(size_t)i * ldr + j] * s_inv[tx];
+    }
+}
+
+static unsigned grid_for(long long work, int per = 256 * 4)
+{
+    long long g = cdiv(work, per);
+    if (g < 1) g = 1;
+    if (g > 65535) g = 65535;
+    return (unsigned)g;
+}
+
+template <bool MN_A>
+static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm, dim3 grid, const PassArgs& pa,
+                               cudaStream_t st)
+{
+    static bool attr[2] = {false, false};
+    auto k = vec ? dion_pass_kernel<MN_A, true> : dion_pass_kernel<MN_A, false>;
+    if (!attr[vec]) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPassSmem);
+        if (e != cudaSuccess) return e;
+        attr[vec] = true;
+    }
+    return launch(name, k, grid, dim3(288), kPassSmem, st, tm, pa);
+}
+
+dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* Gv, float* M, float* Q, float mu,
+                         float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st)
+{
+    bf16* X = (bf16*)Xv;
+    const bf16* G = (const bf16*)Gv;
+    const int rp = L.rp;
+    int* status = (int*)(ws + L.status);
+    float* part = (float*)(ws + L.Ppart);
+    float* P0 = (float*)(ws + L.P0);
+    float* P1 = (float*)(ws + L.P1);
+    float* R = (float*)(ws + L.R);
+    float* S = (float*)(ws + L.S);
+    float* W = (float*)(ws + L.W);
+    int* dead = (int*)(ws + L.dead);
+    float* inv = (float*)(ws + L.inv);
+    bf16* Qt16 = (bf16*)(ws + L.Qt16);
+    bf16* P16 = (bf16*)(ws + L.P16);
+    bf16* R16 = (bf16*)(ws + L.R16);
+    bf16* Q16 = (bf16*)(ws + L.Q16);
+    const long long np = (long long)align_up((size_t)n, 8);
+    const bool vec = (n % 8) == 0;
+    const int rchunks = (int)cdiv(rp, 256);
+    const int nbox = rp < 256 ? rp : 256;
+
+    DION_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
+    // 1. Qt = bf16(Q^T)
+    DION_TRY(launch("dion_prep_qt", dion_prep_qt_kernel, dim3((unsigned)cdiv(n, 32), (unsigned)cdiv(rp, 32), batch),
+                    dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16));
+    // 2. P partials = B Q
+    CUtensorMap tmQt;
+    if (!make_tmap_3d(&tmQt, Qt16, TmapType::BF16, n, rp, batch, np * 2, rp * np * 2, 64, nbox)) return DION_ERR_CUDA;
+    {
+        const int kchunks = (int)cdiv(n, kBK);
+        const int kcps = (int)cdiv(kchunks, L.ksplit);
+        const int splits = (int)cdiv(kchunks, kcps);
+        PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
+        DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, dim3((unsigned)cdiv(m, kBM), splits * rchunks, batch),
+                                    pa, st));
+        const long long cnt = (long long)batch * m * rp;
+        DION_TRY(launch("dion_reduce_p", dion_reduce_kernel, dim3(grid_for(cnt / 4)), dim3(256), 0, st, cnt, splits,
+                        (const float*)part, P0));
+    }
+    // 4. CholeskyQR2 on P (first r columns; padded columns stay zero)
+    DION_TRY(qr_cholesky2(batch, m, r, rp, P0, P1, S, W, dead, status, st));
+    // 5. P16 = bf16(P)
+    DION_TRY(launch("dion_prep_p", dion_to_bf16_kernel, dim3(grid_for((long long)batch * m * rp)), dim3(256), 0, st,
+                    (long long)batch * m, m, r, rp, (const float*)P0, (const float*)nullptr, P16));
+    // 6. R partials = B^T P
+    CUtensorMap tmP64;
+    if (!make_tmap_3d(&tmP64, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
+        return DION_ERR_CUDA;
+    {
+        const int kchunks = (int)cdiv(m, kBK);
+        const int kcps = (int)cdiv(kchunks, L.ksplit_r);
+        const int splits = (int)cdiv(kchunks, kcps);
+        PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
+        DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, dim3((unsigned)cdiv(n, kBM), splits * rchunks, batch),
+                                   pa, st));
+        const long long cnt = (long long)batch * n * rp;
+        DION_TRY(launch("dion_reduce_r", dion_reduce_kernel, dim3(grid_for(cnt / 4)), dim3(256), 0, st, cnt, splits,
+                        (const float*)part, R));
+    }
+    // 7. Q = R / ||R_j||
+    DION_TRY(launch("dion_colnorm", dion_colnorm_tc_kernel, dim3((unsigned)cdiv(r, 32), batch), dim3(32, 8), 0, st, n,
+                    r, (long long)rp, (const float*)R, Q, inv, 1e-12f * sqrtf((float)n), status));
+    // 8. R16, Q16
+    DION_TRY(launch("dion_prep_r", dion_to_bf16_kernel, dim3(grid_for((long long)batch * n * rp)), dim3(256), 0, st,
+                    (long long)batch * n, n, r, rp, (const float*)R, (const float*)nullptr, R16));
+    DION_TRY(launch("dion_prep_q", dion_to_bf16_kernel, dim3(grid_for((long long)batch * n * rp)), dim3(256), 0, st,
+                    (long long)batch * n, n, r, rp, (const float*)R, (const float*)inv, Q16));
+    // 9. M and X updates
+    CUtensorMap tmPa, tmR, tmQ;
+    if (!make_tmap_3d(&tmPa, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||
+        !make_tmap_3d(&tmR, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN) ||
+        !make_tmap_3d(&tmQ, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN))
+        return DION_ERR_CUDA;
+    {
+        static bool attr[2] = {false, false};
+        auto k = vec ? dion_update_tc_kernel<true> : dion_update_tc_kernel<false>;
+        if (!attr[vec]) {
+            DION_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUpdSmem));
+            attr[vec] = true;
+        }
+        UpdArgs ua{m, n, rp, (int)cdiv(rp, kBK), M, G, X, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n),
+                   status};
+        DION_TRY(launch("dion_update_tc", k, dim3((unsigned)cdiv(n, kUBN), (unsigned)cdiv(m, kBM), batch), dim3(192),
+                        kUpdSmem, st, tmPa, tmR, tmQ, ua));
+    }
+    return DION_OK;
+}
+
+}  // namespace dion

@@ -7,10 +7,11 @@ namespace dion {
 
 // Workspace layout of dion_step_batched (byte offsets, each 256-aligned).
 struct DionLayout {
-    int rp;                 // r rounded up for the tensor-core path (== r on the fp32 path)
+    int rp;                 // r rounded up to 64 on the tensor-core path (== r on the fp32 path)
     bool tc;                // tensor-core (bf16) path
-    int ksplit;             // split of the B Q contraction (partials in Ppart)
-    size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Ps16, nrm2, total;
+    int ksplit;             // splits of the B Q contraction over n (partials in Ppart)
+    int ksplit_r;           // splits of the B^T P contraction over m
+    size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Q16, total;
 };
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
 
@@ -18,6 +19,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
 struct MuonLayout {
     int heads, hd, s, l, nb;   // blocks per matrix, block width, Gram side, long side, total blocks
     bool tr, tc;               // blocks transposed (m > hd); tensor-core path
+    int lp, sp;                // row pitches (elements) of the bf16 s x l and l x s / s x s buffers
     size_t status, nrm, Xa, Xb, XTa, XTb, A, Bm, total;
 };
 MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt);
@@ -30,6 +32,11 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
 dion_status dion_step_simt(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
                            float* Q, float mu, float lr, float wd, char* ws, const DionLayout& L,
                            cudaStream_t st);
+dion_status dion_step_tc(int batch, int m, int n, int r, void* X, const void* G, float* M, float* Q, float mu,
+                         float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st);
+dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void* G, float* M, void* O, int steps,
+                    const float* coeff, float mu, float lr, float wd, char* ws, const MuonLayout& L,
+                    cudaStream_t st);
 dion_status muon_simt(int batch, int m, int n, dion_dtype dt, void* X, const void* G, float* M, void* O,
                       int steps, const float* coeff, float mu, float lr, float wd, char* ws,
                       const MuonLayout& L, cudaStream_t st);

@@ -1,0 +1,222 @@
+// tc_gemm.cuh -- persistent batched bf16 GEMM on the 5th-generation tensor
+// cores (tcgen05.mma, accumulator in tensor memory), fed by TMA.
+//
+//   C[b] (M x N) = alpha * aux[b] + beta * (A[b] (M x K) . B[b] (N x K)^T)
+//
+// Both operands are K-major (row-major with K contiguous).  One CTA per SM
+// walks the output tiles (BM = 128 rows, BN = 64/128/256 columns) of every
+// matrix of the batch.  Warp 0 issues TMA loads into a ring of shared-memory
+// stages, warp 1 issues tcgen05.mma from one thread into a double-buffered
+// TMEM accumulator, warps 2..5 drain the accumulator (tcgen05.ld), apply the
+// epilogue and store bf16 results (optionally also the transpose), so the
+// epilogue of one tile overlaps the MMAs of the next.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace dion {
+
+struct TcGemmEpi {
+    int M, N;                       // valid output extent of one matrix
+    int tiles_m, tiles_n, batch;
+    bf16* C; long long ldc, sc;     // output, row pitch and matrix pitch (elements)
+    const bf16* aux; long long ldaux, saux;   // optional addend (same shape as C)
+    bf16* CT; long long ldct, sct;  // optional transposed copy of the output (N x M)
+    float alpha, beta;
+    int* status;
+};
+
+template <int BN>
+struct TcGemmCfg {
+    static constexpr int BM = 128, BK = 64;
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+__device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row, int col0, const uint32_t (&v)[32])
+{
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = ep.beta * __uint_as_float(v[i]);
+    const int ncol = min(32, ep.N - col0);
+    if (ep.aux) {
+        const bf16* ap = ep.aux + b * ep.saux + (long long)row * ep.ldaux + col0;
+        if (ncol == 32) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 u = *reinterpret_cast<const uint4*>(ap + 8 * j);
+                const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[8 * j + e] = fmaf(ep.alpha, __bfloat162float(h[e]), acc[8 * j + e]);
+            }
+        } else {
+            for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, __bfloat162float(ap[i]), acc[i]);
+        }
+    }
+    bf16* cp = ep.C + b * ep.sc + (long long)row * ep.ldc + col0;
+    if (ncol == 32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 u;
+            u.x = tc::pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+            u.y = tc::pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+            u.z = tc::pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+            u.w = tc::pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+            *reinterpret_cast<uint4*>(cp + 8 * j) = u;
+        }
+    } else {
+        for (int i = 0; i < ncol; ++i) cp[i] = __float2bfloat16_rn(acc[i]);
+    }
+    if (ep.CT) {
+        bf16* tp = ep.CT + b * ep.sct + (long long)col0 * ep.ldct + row;
+        for (int i = 0; i < ncol; ++i) tp[(long long)i * ep.ldct] = __float2bfloat16_rn(acc[i]);
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int K, TcGemmEpi ep)
+{
+    using Cfg = TcGemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty = full + Cfg::STAGES;
+    uint64_t* acc_full = empty + Cfg::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    volatile int* abrt = abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&acc_full[b], 1);
+            tc::mbar_init(&acc_empty[b], 4);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int per_mat = ep.tiles_m * ep.tiles_n;
+    const int tiles = ep.batch * per_mat;
+    const int kchunks = (K + Cfg::BK - 1) / Cfg::BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmA);
+            tc::tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
+                const int b = t / per_mat, rem = t % per_mat;
+                const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+                for (int kc = 0; kc < kchunks; ++kc) {
+                    if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) break;
+                    uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+                    tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, b);
+                    tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, b);
+                    if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::make_idesc(Cfg::BM, BN, 1, false, false);
+            int stage = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+                const int buf = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!tc::mbar_wait(&acc_empty[buf], aph ^ 1, abrt, ep.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + buf * BN;
+                bool ok = true;
+                for (int kc = 0; kc < kchunks; ++kc) {
+                    if (!tc::mbar_wait(&full[stage], ph, abrt, ep.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                    const uint32_t b0 = a0 + Cfg::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k)
+                        tc::mma_bf16(d, tc::make_sdesc(a0 + k * 32, 16, 1024), tc::make_sdesc(b0 + k * 32, 16, 1024),
+                                     idesc, (kc | k) != 0);
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(&acc_full[buf]);
+            }
+        }
+    } else {
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        int it = 0;
+        for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+            const int buf = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!tc::mbar_wait(&acc_full[buf], aph, abrt, ep.status)) break;
+            tc::tc_fence_after();
+            const int b = t / per_mat, rem = t % per_mat;
+            const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+            const int row = tm * Cfg::BM + q * 32 + lane;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
+                tc::tmem_ld_wait();
+                const int col0 = tn * BN + c0;
+                if (row < ep.M && col0 < ep.N) tc_epi_store(ep, b, row, col0, v);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+int num_sms();
+
+// Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN.
+template <int BN>
+cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
+                    cudaStream_t st)
+{
+    using Cfg = TcGemmCfg<BN>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int tiles = ep.batch * ep.tiles_m * ep.tiles_n;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    return launch(name, tc_gemm_kernel<BN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
+}
+
+}  // namespace dion
