@@ -9,95 +9,162 @@
 // application are batched GEMMs; the r x r factorization runs one CTA per
 // matrix.
 //
-// Rank deficiency: a pivot d <= r * 6e-8 * max(diag S) (or non-finite) marks
-// column j dependent.  Its column of L is zeroed and its column of L^{-T} is
-// set to zero, so the corresponding column of the new P is exactly zero and
-// the remaining columns stay orthonormal; the status word records the event.
+// Rank deficiency: a pivot d <= 1e-6 * S_jj (the column's own squared norm;
+// d / S_jj is the squared sine of its angle to the span of the columns before
+// it), or a non-finite pivot, marks column j dependent.  Its column of L is
+// zeroed and its column of L^{-T} is set to zero, so the corresponding column
+// of the new P is exactly zero and the remaining columns stay orthonormal; the
+// status word records the event.
 #include "internal.h"
 #include "simt_gemm.cuh"
 
 namespace dion {
 
+// One CTA per matrix: Cholesky S = L L^T and W = L^{-T}, both blocked by 32.
+//   Cholesky (right-looking), per 32-column block J:
+//     warp 0 factors the diagonal block (lane = row, shuffles for the pivot),
+//     one thread per row solves the panel below it,
+//     the trailing lower triangle is updated with one warp per row.
+//   Inverse Z = L^{-1} (lower), written transposed as W = Z^T:
+//     diagonal blocks Z_II = L_II^{-1} (one warp each, registers),
+//     then block diagonals d = 1, 2, ...: Z_IJ = -Z_II sum_{K=J}^{I-1} L_IK Z_KJ,
+//     with the partial sums parked in the (finally zeroed) lower part of W.
+// kSmem: L lives in shared memory with row pitch r + 1 (no bank conflicts);
+// otherwise it is factored in place in global memory (pitch r).
 template <bool kSmem>
 __global__ void __launch_bounds__(1024) chol_inv_kernel(int r, float* S, float* W, int* dead_g, int* status)
 {
     extern __shared__ float smem[];
-    __shared__ float s_piv, s_thr;
-    __shared__ int s_dead, s_bad;
-    const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    __shared__ int s_bad;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    const int nwarps = nt >> 5;
     float* Sg = S + (size_t)b * r * r;
     float* Wg = W + (size_t)b * r * r;
     int* dead = dead_g + (size_t)b * r;
+    const int ld = kSmem ? r + 1 : r;
     float* L = kSmem ? smem : Sg;
+    float* d0 = kSmem ? smem + (size_t)r * ld : smem;     // original diagonal
     if (kSmem)
-        for (int e = tid; e < r * r; e += nt) L[e] = Sg[e];
+        for (int e = tid; e < r * r; e += nt) L[(size_t)(e / r) * ld + (e % r)] = Sg[e];
+    for (int i = tid; i < r; i += nt) d0[i] = Sg[(size_t)i * r + i];
+    if (tid == 0) s_bad = 0;
     __syncthreads();
-    if (tid == 0) {
-        float mx = 0.f;
-        for (int i = 0; i < r; ++i) {
-            const float d = L[(size_t)i * r + i];
-            if (d > mx) mx = d;
-        }
-        s_thr = mx * (float)r * 6e-8f;
-        s_bad = 0;
-    }
-    __syncthreads();
-    for (int j = 0; j < r; ++j) {
-        if (tid == 0) {
-            const float d = L[(size_t)j * r + j];
-            const bool fin = isfinite(d);
-            const bool ok = fin && d > s_thr;
-            if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
-            s_dead = !ok;
-            s_piv = ok ? sqrtf(d) : 1.f;
-            L[(size_t)j * r + j] = s_piv;
-            dead[j] = !ok;
+#define Lx(i, k) L[(size_t)(i) * ld + (k)]
+
+    for (int J = 0; J < r; J += 32) {
+        const int jb = min(32, r - J);
+        if (warp == 0) {
+            for (int c = 0; c < jb; ++c) {
+                float d = (lane == c) ? Lx(J + c, J + c) : 0.f;
+                d = __shfl_sync(0xffffffffu, d, c);
+                const bool fin = isfinite(d);
+                const bool ok = fin && d > 1e-6f * d0[J + c];
+                const float piv = ok ? sqrtf(d) : 1.f;
+                if (lane == 0) {
+                    dead[J + c] = !ok;
+                    if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
+                }
+                if (lane == c) Lx(J + c, J + c) = piv;
+                float lv = 0.f;
+                if (lane > c && lane < jb) {
+                    lv = ok ? Lx(J + lane, J + c) / piv : 0.f;
+                    Lx(J + lane, J + c) = lv;
+                }
+                __syncwarp();
+                if (ok && lane > c && lane < jb)
+                    for (int k = c + 1; k <= lane; ++k) Lx(J + lane, J + k) -= lv * Lx(J + k, J + c);
+                __syncwarp();
+            }
         }
         __syncthreads();
-        const float piv = s_piv;
-        const int dj = s_dead;
-        for (int i = j + 1 + tid; i < r; i += nt) {
-            float* p = &L[(size_t)i * r + j];
-            *p = dj ? 0.f : *p / piv;
+        for (int i = J + jb + tid; i < r; i += nt) {
+            for (int c = 0; c < jb; ++c) {
+                float s = Lx(i, J + c);
+                for (int k = 0; k < c; ++k) s -= Lx(i, J + k) * Lx(J + c, J + k);
+                Lx(i, J + c) = dead[J + c] ? 0.f : s / Lx(J + c, J + c);
+            }
         }
         __syncthreads();
-        const int w = r - j - 1;
-        if (!dj) {
-            for (int e = tid; e < w * w; e += nt) {
-                const int ii = j + 1 + e / w, kk = j + 1 + e % w;
-                if (kk <= ii) L[(size_t)ii * r + kk] -= L[(size_t)ii * r + j] * L[(size_t)kk * r + j];
+        const int t0 = J + jb;
+        for (int i = t0 + warp; i < r; i += nwarps) {
+            for (int k = t0 + lane; k <= i; k += 32) {
+                float s = 0.f;
+                for (int c = 0; c < jb; ++c) s = fmaf(Lx(i, J + c), Lx(k, J + c), s);
+                Lx(i, k) -= s;
             }
         }
         __syncthreads();
     }
-    // W = L^{-T}: row c of W is column c of L^{-1} (forward substitution).
-    for (int c = tid; c < r; c += nt) {
-        float* wrow = Wg + (size_t)c * r;
-        for (int i = 0; i < c; ++i) wrow[i] = 0.f;
-        for (int i = c; i < r; ++i) {
+
+    // ---- inverse: W = L^{-T}
+    const int nb = (r + 31) / 32;
+#define Wx(i, k) Wg[(size_t)(i) * r + (k)]
+    for (int I = warp; I < nb; I += nwarps) {
+        const int I0 = I * 32, ib = min(32, r - I0);
+        const int c = lane;
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
             float s = (i == c) ? 1.f : 0.f;
-            for (int k = c; k < i; ++k) s -= L[(size_t)i * r + k] * wrow[k];
-            wrow[i] = dead[i] ? 0.f : s / L[(size_t)i * r + i];
+#pragma unroll
+            for (int k = 0; k < i; ++k)
+                if (k >= c) s = fmaf(-Lx(I0 + i, I0 + k), z[k], s);
+            const bool valid = i >= c && i < ib && c < ib;
+            z[i] = (valid && !dead[I0 + i]) ? s / Lx(I0 + i, I0 + i) : 0.f;
         }
+        if (c < ib)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ib) Wx(I0 + c, I0 + i) = z[i];          // W[c][i] = Z[i][c]
     }
+    __syncthreads();
+    for (int d = 1; d < nb; ++d) {
+        // T_IJ = sum_{K=J}^{I-1} L_IK Z_KJ  -> parked at W block (I, J)
+        for (int e = tid; e < (nb - d) * 1024; e += nt) {
+            const int I = d + e / 1024, J = I - d, a = (e % 1024) / 32, bb = e % 32;
+            const int I0 = I * 32, J0 = J * 32;
+            if (I0 + a >= r || J0 + bb >= r) continue;
+            float s = 0.f;
+            for (int k = J0; k < I0; ++k) s = fmaf(Lx(I0 + a, k), Wx(J0 + bb, k), s);   // Z[k][J0+bb] = W[J0+bb][k]
+            Wx(I0 + a, J0 + bb) = s;
+        }
+        __syncthreads();
+        // Z_IJ = -Z_II T_IJ  -> W block (J, I)
+        for (int e = tid; e < (nb - d) * 1024; e += nt) {
+            const int I = d + e / 1024, J = I - d, a = (e % 1024) / 32, bb = e % 32;
+            const int I0 = I * 32, J0 = J * 32;
+            if (I0 + a >= r || J0 + bb >= r) continue;
+            float s = 0.f;
+            for (int k = 0; k <= a; ++k) s = fmaf(Wx(I0 + k, I0 + a), Wx(I0 + k, J0 + bb), s);  // Z_II[a][k] = W[I0+k][I0+a]
+            Wx(J0 + bb, I0 + a) = dead[I0 + a] ? 0.f : -s;
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < r * r; e += nt) {
+        const int i = e / r, k = e % r;
+        if (k < i) Wx(i, k) = 0.f;
+    }
+#undef Wx
+#undef Lx
     if (tid == 0 && s_bad) atomicOr(status, s_bad);
 }
 
 static cudaError_t chol_inv(int batch, int r, float* S, float* W, int* dead, int* status, cudaStream_t st)
 {
-    const size_t smem = (size_t)r * r * sizeof(float);
-    if (smem <= 200 * 1024) {
+    const size_t smem = ((size_t)r * (r + 1) + r) * sizeof(float);
+    if (smem <= 210 * 1024) {
         static bool attr = false;
         if (!attr) {
             cudaError_t e = cudaFuncSetAttribute(chol_inv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 200 * 1024);
+                                                 210 * 1024);
             if (e != cudaSuccess) return e;
             attr = true;
         }
         return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(1024), smem, st, r, S, W, dead,
                       status);
     }
-    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(1024), 0, st, r, S, W, dead, status);
+    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(1024), (size_t)r * sizeof(float), st,
+                  r, S, W, dead, status);
 }
 
 cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,

@@ -45,7 +45,8 @@ RAGGED = [
     (2, 200, 136, 136, torch.bfloat16),    # r = n = min(m, n)
     (1, 97, 131, 1, torch.float32),        # r = 1, odd sizes
     (2, 130, 260, 17, torch.bfloat16),
-    (1, 64, 64, 64, torch.bfloat16),
+    (1, 64, 64, 16, torch.bfloat16),
+    (2, 384, 320, 320, torch.bfloat16),    # r = n = min(m, n), r > 256 (two 256-column chunks)
     (1, 8, 520, 3, torch.bfloat16),        # very wide
     (2, 520, 8, 8, torch.float32),         # very tall, full rank
 ]
