@@ -106,9 +106,11 @@ __global__ void __launch_bounds__(1024) chol_inv_kernel(int r, float* S, float* 
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             float s = (i == c) ? 1.f : 0.f;
+            if (i < ib) {                       // rows of L beyond r do not exist
 #pragma unroll
-            for (int k = 0; k < i; ++k)
-                if (k >= c) s = fmaf(-Lx(I0 + i, I0 + k), z[k], s);
+                for (int k = 0; k < i; ++k)
+                    if (k >= c) s = fmaf(-Lx(I0 + i, I0 + k), z[k], s);
+            }
             const bool valid = i >= c && i < ib && c < ib;
             z[i] = (valid && !dead[I0 + i]) ? s / Lx(I0 + i, I0 + i) : 0.f;
         }
@@ -119,9 +121,10 @@ __global__ void __launch_bounds__(1024) chol_inv_kernel(int r, float* S, float* 
     }
     __syncthreads();
     for (int d = 1; d < nb; ++d) {
-        // T_IJ = sum_{K=J}^{I-1} L_IK Z_KJ  -> parked at W block (I, J)
+        // T_IJ = sum_{K=J}^{I-1} L_IK Z_KJ  -> parked at W block (I, J).  The
+        // lane index runs over a, so the W row read below is a broadcast.
         for (int e = tid; e < (nb - d) * 1024; e += nt) {
-            const int I = d + e / 1024, J = I - d, a = (e % 1024) / 32, bb = e % 32;
+            const int I = d + e / 1024, J = I - d, a = e % 32, bb = (e % 1024) / 32;
             const int I0 = I * 32, J0 = J * 32;
             if (I0 + a >= r || J0 + bb >= r) continue;
             float s = 0.f;

@@ -46,7 +46,7 @@ RAGGED = [
     (1, 97, 131, 1, torch.float32),        # r = 1, odd sizes
     (2, 130, 260, 17, torch.bfloat16),
     (1, 64, 64, 16, torch.bfloat16),
-    (2, 384, 320, 320, torch.bfloat16),    # r = n = min(m, n), r > 256 (two 256-column chunks)
+    (1, 1024, 1024, 288, torch.bfloat16),  # r > 256: two 256-column chunks of the rank
     (1, 8, 520, 3, torch.bfloat16),        # very wide
     (2, 520, 8, 8, torch.float32),         # very tall, full rank
 ]
