@@ -22,9 +22,10 @@ namespace dion {
 
 // One CTA per matrix: Cholesky S = L L^T and W = L^{-T}, both blocked by 32.
 //   Cholesky (right-looking), per 32-column block J:
-//     warp 0 factors the diagonal block (lane = row, shuffles for the pivot),
-//     one thread per row solves the panel below it,
-//     the trailing lower triangle is updated with one warp per row.
+//     warp 0 factors the diagonal block in registers (lane = row; columns
+//     are broadcast with shuffles), one thread per row solves the panel below
+//     it in registers, and the trailing lower triangle is updated with one
+//     warp per row.
 //   Inverse Z = L^{-1} (lower), written transposed as W = Z^T:
 //     diagonal blocks Z_II = L_II^{-1} (one warp each, registers),
 //     then block diagonals d = 1, 2, ...: Z_IJ = -Z_II sum_{K=J}^{I-1} L_IK Z_KJ,
@@ -32,7 +33,7 @@ namespace dion {
 // kSmem: L lives in shared memory with row pitch r + 1 (no bank conflicts);
 // otherwise it is factored in place in global memory (pitch r).
 template <bool kSmem>
-__global__ void __launch_bounds__(1024) chol_inv_kernel(int r, float* S, float* W, int* dead_g, int* status)
+__global__ void __launch_bounds__(512) chol_inv_kernel(int r, float* S, float* W, int* dead_g, int* status)
 {
     extern __shared__ float smem[];
     __shared__ int s_bad;
@@ -54,42 +55,66 @@ __global__ void __launch_bounds__(1024) chol_inv_kernel(int r, float* S, float* 
     for (int J = 0; J < r; J += 32) {
         const int jb = min(32, r - J);
         if (warp == 0) {
-            for (int c = 0; c < jb; ++c) {
-                float d = (lane == c) ? Lx(J + c, J + c) : 0.f;
-                d = __shfl_sync(0xffffffffu, d, c);
-                const bool fin = isfinite(d);
-                const bool ok = fin && d > 1e-6f * d0[J + c];
-                const float piv = ok ? sqrtf(d) : 1.f;
-                if (lane == 0) {
-                    dead[J + c] = !ok;
-                    if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
+            // diagonal block in registers: lane = row, a[k] = L(J + lane, J + k)
+            float a[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) a[k] = (lane < jb && k < jb) ? Lx(J + lane, J + k) : 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                if (c < jb) {
+                    const float d = __shfl_sync(0xffffffffu, a[c], c);
+                    const bool fin = isfinite(d);
+                    const bool ok = fin && d > 1e-6f * d0[J + c];
+                    const float piv = ok ? sqrtf(d) : 1.f;
+                    if (lane == 0) {
+                        dead[J + c] = !ok;
+                        if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
+                    }
+                    const float lv = (lane > c) ? (ok ? a[c] / piv : 0.f) : (lane == c ? piv : a[c]);
+                    a[c] = lv;
+#pragma unroll
+                    for (int k = c + 1; k < 32; ++k) {
+                        const float lkc = __shfl_sync(0xffffffffu, lv, k);     // L(J + k, J + c)
+                        if (lane >= k && lane > c) a[k] = fmaf(-lv, lkc, a[k]);
+                    }
                 }
-                if (lane == c) Lx(J + c, J + c) = piv;
-                float lv = 0.f;
-                if (lane > c && lane < jb) {
-                    lv = ok ? Lx(J + lane, J + c) / piv : 0.f;
-                    Lx(J + lane, J + c) = lv;
-                }
-                __syncwarp();
-                if (ok && lane > c && lane < jb)
-                    for (int k = c + 1; k <= lane; ++k) Lx(J + lane, J + k) -= lv * Lx(J + k, J + c);
-                __syncwarp();
             }
+            if (lane < jb)
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (k < jb) Lx(J + lane, J + k) = a[k];
         }
         __syncthreads();
+        // panel below the diagonal block: one thread per row, row held in registers
         for (int i = J + jb + tid; i < r; i += nt) {
-            for (int c = 0; c < jb; ++c) {
-                float s = Lx(i, J + c);
-                for (int k = 0; k < c; ++k) s -= Lx(i, J + k) * Lx(J + c, J + k);
-                Lx(i, J + c) = dead[J + c] ? 0.f : s / Lx(J + c, J + c);
+            float a[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) a[c] = (c < jb) ? Lx(i, J + c) : 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                if (c < jb) {
+                    float s = a[c];
+#pragma unroll
+                    for (int k = 0; k < c; ++k) s = fmaf(-a[k], Lx(J + c, J + k), s);
+                    a[c] = dead[J + c] ? 0.f : s / Lx(J + c, J + c);
+                }
             }
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < jb) Lx(i, J + c) = a[c];
         }
         __syncthreads();
+        // trailing lower triangle: one warp per row i, lanes over k
         const int t0 = J + jb;
         for (int i = t0 + warp; i < r; i += nwarps) {
+            float li[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) li[c] = (c < jb) ? Lx(i, J + c) : 0.f;
             for (int k = t0 + lane; k <= i; k += 32) {
                 float s = 0.f;
-                for (int c = 0; c < jb; ++c) s = fmaf(Lx(i, J + c), Lx(k, J + c), s);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (c < jb) s = fmaf(li[c], Lx(k, J + c), s);
                 Lx(i, k) -= s;
             }
         }
@@ -163,10 +188,10 @@ static cudaError_t chol_inv(int batch, int r, float* S, float* W, int* dead, int
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(1024), smem, st, r, S, W, dead,
+        return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, S, W, dead,
                       status);
     }
-    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(1024), (size_t)r * sizeof(float), st,
+    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(512), (size_t)r * sizeof(float), st,
                   r, S, W, dead, status);
 }
 
