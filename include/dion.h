@@ -95,6 +95,40 @@ dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt,
                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Upper bound, in bytes, of the fixed device scratch of
+ * dion_step_batched_static (64 MiB).  Every GPU that loads libdion holds an
+ * array of this size until the process exits.
+ */
+#define DION_STATIC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * dion_step_batched without a workspace argument: the step's scratch memory is
+ * a fixed array inside libdion, so the call allocates nothing.  The pages have
+ * no counterpart of this entry point; it exists for callers that cannot call
+ * cudaMalloc: code whose device memory is all owned by another allocator (a
+ * framework's caching pool, or one arena reserved at start-up) and may not
+ * take more, and code on a latency-critical path where an allocation, which
+ * can synchronize the device, is not acceptable.  The caller still passes
+ * X, G, M and Q, with the meaning, layout and in-place updates of
+ * dion_step_batched, and the results are those of dion_step_batched.
+ *   - Shapes whose dion_workspace_size exceeds DION_STATIC_SCRATCH_BYTES are
+ *     rejected with DION_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture, and not from two threads at once.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (the step clears what must start at zero itself).  Calls that
+ *     overlap on the GPU (on different streams, or from different threads)
+ *     race on it and give wrong results: serialize them.
+ *   - The status word is not readable by the caller for this variant; a
+ *     numeric breakdown still yields finite output (dependent columns of P
+ *     are zeroed) as for dion_step_batched.
+ */
+dion_status dion_step_batched_static(int batch, int m, int n, int r, dion_dtype dt,
+                                     void* X, const void* G, float* M, float* Q,
+                                     float mu, float lr, float weight_decay, void* cuda_stream);
+
+/*
  * Where this step's panels live inside a dion_step_batched workspace, for
  * callers that want the low-rank factors themselves (diagnostics, or a
  * compressed data-parallel exchange of P and R).  After a step on the

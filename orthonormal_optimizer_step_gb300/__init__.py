@@ -24,7 +24,7 @@ DION_OK, DION_ERR_INVALID_ARG, DION_ERR_UNSUPPORTED, DION_ERR_WORKSPACE, DION_ER
 DION_F32, DION_BF16 = 0, 1
 
 # The exported symbols of include/dion.h.
-EXPORTS = ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "muon_workspace_size", "muon_ns_batched",
+EXPORTS = ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
            "dion_get_status", "dion_status_string", "dion_profile_begin", "dion_profile_end",
            "dion_profile_count", "dion_profile_entry")
 
@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         L.dion_workspace_panels.argtypes = [c_int] * 5 + [ctypes.POINTER(c_size), ctypes.POINTER(c_int),
                                                           ctypes.POINTER(c_size), ctypes.POINTER(c_int)]
         L.dion_step_batched.argtypes = ([c_int] * 5 + [vp, vp, vp, vp] + [c_float] * 3 + [vp, c_size, vp])
+        L.dion_step_batched_static.argtypes = ([c_int] * 5 + [vp, vp, vp, vp] + [c_float] * 3 + [vp])
         L.muon_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]
         L.muon_ns_batched.argtypes = ([c_int] * 5 + [vp, vp, vp, vp, c_int, ctypes.POINTER(c_float)]
                                       + [c_float] * 3 + [vp, c_size, vp])
@@ -66,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.dion_profile_count.argtypes = []
         L.dion_profile_entry.argtypes = [c_int, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_int),
                                          ctypes.POINTER(ctypes.c_double)]
-        for f in ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "muon_workspace_size", "muon_ns_batched",
+        for f in ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
                   "dion_get_status", "dion_profile_begin", "dion_profile_end", "dion_profile_count",
                   "dion_profile_entry"):
             getattr(L, f).restype = c_int
@@ -165,6 +166,26 @@ def dion_step_batched(X, G, M, Q, *, mu: float, lr: float, weight_decay: float =
                                    float(weight_decay), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(code, "dion_step_batched")
     return workspace
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def dion_step_batched_static(X, G, M, Q, *, mu: float, lr: float, weight_decay: float = 0.0, stream=None):
+    """dion_step_batched for callers that cannot allocate device memory: the
+    scratch is a fixed array of STATIC_SCRATCH_BYTES inside libdion, shared by
+    all calls on a device (serialize them).  Shapes needing more scratch raise
+    DionError (DION_ERR_WORKSPACE).  The first call on a device sets up the
+    array's address; make it before any stream capture."""
+    batch, m, n = _shape3(X)
+    r = Q.shape[-1]
+    dt = _dtype_code(X)
+    for t in (X, G, M, Q):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    code = lib().dion_step_batched_static(batch, m, n, r, dt, _ptr(X), _ptr(G), _ptr(M), _ptr(Q), float(mu),
+                                          float(lr), float(weight_decay), _stream_ptr(stream))
+    _check(code, "dion_step_batched_static")
 
 
 def muon_ns_batched(G, *, X=None, M=None, O=None, head_dim: int = 0, steps: int = 5,
