@@ -51,8 +51,13 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.P16 = carve(off, b * m * rp * h);
         L.R16 = carve(off, b * n * rp * h);
         L.Q16 = carve(off, b * n * rp * h);
+        L.T3 = carve(off, 3 * b * rp * align_up((size_t)m, 8) * h);
+        L.P3 = carve(off, 3 * b * m * rp * h);
+        L.Z3 = carve(off, 3 * b * r * rp * h);
+        L.S6 = carve(off, 6 * b * r * r * f);
     } else {
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
+        L.T3 = L.P3 = L.Z3 = L.S6 = off;
     }
     L.total = off;
     return L;

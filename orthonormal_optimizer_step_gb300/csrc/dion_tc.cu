@@ -7,7 +7,8 @@
 //                      bf16 and written straight into the swizzled MMA operand
 //                      tile (B is never stored); split over n, fp32 partials
 //   3. dion_reduce   : P = sum of partials
-//   4. CholeskyQR2 of P (float32)
+//   4. CholeskyQR2 of P (float32 accuracy; products on the tensor cores,
+//      qr_tc.cu)
 //   5. dion_prep_p   : P16 = bf16(P)
 //   6. dion_btp_tc   : R = B^T P, contracting over m: both operands are read
 //                      MN-major (B rows are K rows), so B is again formed in
@@ -471,9 +472,6 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     float* P0 = (float*)(ws + L.P0);
     float* P1 = (float*)(ws + L.P1);
     float* R = (float*)(ws + L.R);
-    float* S = (float*)(ws + L.S);
-    float* W = (float*)(ws + L.W);
-    int* dead = (int*)(ws + L.dead);
     float* inv = (float*)(ws + L.inv);
     bf16* Qt16 = (bf16*)(ws + L.Qt16);
     bf16* P16 = (bf16*)(ws + L.P16);
@@ -503,7 +501,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
                         (const float*)part, P0));
     }
     // 4. CholeskyQR2 on P (first r columns; padded columns stay zero)
-    DION_TRY(qr_cholesky2(batch, m, r, rp, P0, P1, S, W, dead, status, st));
+    DION_TRY(qr_cholesky2_tc(batch, m, r, rp, P0, P1, ws, L, status, st));
     // 5. P16 = bf16(P)
     DION_TRY(launch("dion_prep_p", dion_to_bf16_kernel, dim3(grid_for((long long)batch * m * rp)), dim3(256), 0, st,
                     (long long)batch * m, m, r, rp, (const float*)P0, (const float*)nullptr, P16));

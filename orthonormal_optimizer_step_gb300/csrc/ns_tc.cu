@@ -149,14 +149,14 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
                   make_tmap_3d(&tYTa_b, YTa, TmapType::BF16, s, l, nb, sp * 2, syt * 2, 64, bn_l);
         if (!ok) return DION_ERR_CUDA;
         // A = Y Y^T
-        TcGemmEpi e1{s, s, tm, (int)cdiv(s, bn_s), nb, A, sp, sa, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status};
+        TcGemmEpi e1{s, s, tm, (int)cdiv(s, bn_s), nb, A, sp, sa, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, nullptr, 1, 1, 0, 0u, 0u};
         DION_TRY(gemm_bn(bn_s, "ns_gram_tc", tYa_a, tYa_b, l, e1, st));
         // Bm = b A + c A A   (A symmetric: A A = A A^T)
         TcGemmEpi e2{s, s, tm, (int)cdiv(s, bn_s), nb, Bm, sp, sa, A, sp, sa, nullptr, 0, 0, coeff[1], coeff[2],
-                     status};
+                     status, nullptr, 1, 1, 0, 0u, 0u};
         DION_TRY(gemm_bn(bn_s, "ns_poly_tc", tA_a, tA_b, s, e2, st));
         // Y' = a Y + Bm Y, written as Y' and Y'^T
-        TcGemmEpi e3{s, l, tm, (int)cdiv(l, bn_l), nb, Yb, lp, sy, Ya, lp, sy, YTb, sp, syt, coeff[0], 1.f, status};
+        TcGemmEpi e3{s, l, tm, (int)cdiv(l, bn_l), nb, Yb, lp, sy, Ya, lp, sy, YTb, sp, syt, coeff[0], 1.f, status, nullptr, 1, 1, 0, 0u, 0u};
         DION_TRY(gemm_bn(bn_l, "ns_axpy_tc", tBm_a, tYTa_b, s, e3, st));
         std::swap(Ya, Yb);
         std::swap(YTa, YTb);

@@ -26,28 +26,43 @@ namespace dion {
 //     are broadcast with shuffles), one thread per row solves the panel below
 //     it in registers, and the trailing lower triangle is updated with one
 //     warp per row.
-//   Inverse Z = L^{-1} (lower), written transposed as W = Z^T:
-//     diagonal blocks Z_II = L_II^{-1} (one warp each, registers),
-//     then block diagonals d = 1, 2, ...: Z_IJ = -Z_II sum_{K=J}^{I-1} L_IK Z_KJ,
-//     with the partial sums parked in the (finally zeroed) lower part of W.
+//   Inverse, in place, block columns from the last to the first: the
+//     diagonal block is inverted in registers (one warp, lane = column), and
+//     the panel below it becomes -(trailing inverse) * panel * (block inverse).
+//   W receives L^{-1} row-major (upper part zero).
 // kSmem: L lives in shared memory with row pitch r + 1 (no bank conflicts);
 // otherwise it is factored in place in global memory (pitch r).
+// Sin holds nparts partial Gram matrices per matrix (summed on load); Swork is
+// the in-place factor of the global variant.  Output: W = L^{-1} as float32
+// (W != NULL), or as three bf16 terms Z3[3b + t] (pitch ldz, columns up to ldz,
+// Z = Z3[0] + Z3[1] + Z3[2] to float32 accuracy) for the tensor-core apply.
 template <bool kSmem>
-__global__ void __launch_bounds__(512) chol_inv_kernel(int r, float* S, float* W, int* dead_g, int* status)
+__global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
+                                                       float* W, bf16* Z3, int ldz, int* dead_g, int* status)
 {
     extern __shared__ float smem[];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
     const int nwarps = nt >> 5;
-    float* Sg = S + (size_t)b * r * r;
-    float* Wg = W + (size_t)b * r * r;
+    const size_t rr = (size_t)r * r;
+    const float* Sb = Sin + (size_t)b * nparts * rr;
+    float* Sg = Swork + (size_t)b * rr;
+    float* Wg = Wbuf + (size_t)b * rr;
     int* dead = dead_g + (size_t)b * r;
     const int ld = kSmem ? r + 1 : r;
     float* L = kSmem ? smem : Sg;
     float* d0 = kSmem ? smem + (size_t)r * ld : smem;     // original diagonal
-    if (kSmem)
-        for (int e = tid; e < r * r; e += nt) L[(size_t)(e / r) * ld + (e % r)] = Sg[e];
-    for (int i = tid; i < r; i += nt) d0[i] = Sg[(size_t)i * r + i];
+    int* deadsm = (int*)(d0 + r);                          // dependent-column flags
+#define Lx0(i) (kSmem ? L[(size_t)(i) * ld + (i)] : Sg[(size_t)(i) * r + (i)])
+    float* T = kSmem ? (float*)(deadsm + r) : Wg;         // (r - 32) x 32 scratch of the inverse
+    for (int e = tid; e < r * r; e += nt) {
+        float v = Sb[e];
+        for (int q = 1; q < nparts; ++q) v += Sb[(size_t)q * rr + e];
+        if (kSmem) L[(size_t)(e / r) * ld + (e % r)] = v;
+        else Sg[e] = v;
+    }
+    __syncthreads();
+    for (int i = tid; i < r; i += nt) d0[i] = Lx0(i);
     if (tid == 0) s_bad = 0;
     __syncthreads();
 #define Lx(i, k) L[(size_t)(i) * ld + (k)]
@@ -96,7 +111,7 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, float* S, float* W
                     float s = a[c];
 #pragma unroll
                     for (int k = 0; k < c; ++k) s = fmaf(-a[k], Lx(J + c, J + k), s);
-                    a[c] = dead[J + c] ? 0.f : s / Lx(J + c, J + c);
+                    a[c] = deadsm[J + c] ? 0.f : s / Lx(J + c, J + c);
                 }
             }
 #pragma unroll
@@ -121,78 +136,100 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, float* S, float* W
         __syncthreads();
     }
 
-    // ---- inverse: W = L^{-T}
-    const int nb = (r + 31) / 32;
-#define Wx(i, k) Wg[(size_t)(i) * r + (k)]
-    for (int I = warp; I < nb; I += nwarps) {
-        const int I0 = I * 32, ib = min(32, r - I0);
-        const int c = lane;
-        float z[32];
+    // ---- in-place inverse L <- L^{-1}, block columns from the last one back:
+    //   Z_JJ = L_JJ^{-1};  panel <- -(L^{-1} of the trailing part) * panel * Z_JJ
+    for (int J = ((r - 1) / 32) * 32; J >= 0; J -= 32) {
+        const int jb = min(32, r - J), t0 = J + jb, nt_rows = r - t0;
+        // T = Linv_trail * panel  (rows t0..r-1, 32 columns), one warp per row
+        for (int i = t0 + warp; i < r; i += nwarps) {
+            float s = 0.f;
+            if (lane < jb)
+                for (int k = t0; k <= i; ++k) s = fmaf(Lx(i, k), Lx(k, J + lane), s);
+            T[(size_t)(i - t0) * 32 + lane] = s;
+        }
+        if (warp == 0) {
+            // Z_JJ: lane c computes column c by forward substitution (registers)
+            const int c = lane;
+            float z[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            float s = (i == c) ? 1.f : 0.f;
-            if (i < ib) {                       // rows of L beyond r do not exist
+            for (int i = 0; i < 32; ++i) {
+                float v = (i == c) ? 1.f : 0.f;
+                if (i < jb) {
 #pragma unroll
-                for (int k = 0; k < i; ++k)
-                    if (k >= c) s = fmaf(-Lx(I0 + i, I0 + k), z[k], s);
+                    for (int k = 0; k < i; ++k)
+                        if (k >= c) v = fmaf(-Lx(J + i, J + k), z[k], v);
+                }
+                z[i] = (i >= c && i < jb && c < jb) ? v / Lx(J + i, J + i) : 0.f;
             }
-            const bool valid = i >= c && i < ib && c < ib;
-            z[i] = (valid && !dead[I0 + i]) ? s / Lx(I0 + i, I0 + i) : 0.f;
-        }
-        if (c < ib)
+            __syncwarp();
+            if (c < jb)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < ib) Wx(I0 + c, I0 + i) = z[i];          // W[c][i] = Z[i][c]
-    }
-    __syncthreads();
-    for (int d = 1; d < nb; ++d) {
-        // T_IJ = sum_{K=J}^{I-1} L_IK Z_KJ  -> parked at W block (I, J).  The
-        // lane index runs over a, so the W row read below is a broadcast.
-        for (int e = tid; e < (nb - d) * 1024; e += nt) {
-            const int I = d + e / 1024, J = I - d, a = e % 32, bb = (e % 1024) / 32;
-            const int I0 = I * 32, J0 = J * 32;
-            if (I0 + a >= r || J0 + bb >= r) continue;
-            float s = 0.f;
-            for (int k = J0; k < I0; ++k) s = fmaf(Lx(I0 + a, k), Wx(J0 + bb, k), s);   // Z[k][J0+bb] = W[J0+bb][k]
-            Wx(I0 + a, J0 + bb) = s;
+                for (int i = 0; i < 32; ++i)
+                    if (i >= c && i < jb) Lx(J + i, J + c) = z[i];
         }
         __syncthreads();
-        // Z_IJ = -Z_II T_IJ  -> W block (J, I)
-        for (int e = tid; e < (nb - d) * 1024; e += nt) {
-            const int I = d + e / 1024, J = I - d, a = (e % 1024) / 32, bb = e % 32;
-            const int I0 = I * 32, J0 = J * 32;
-            if (I0 + a >= r || J0 + bb >= r) continue;
-            float s = 0.f;
-            for (int k = 0; k <= a; ++k) s = fmaf(Wx(I0 + k, I0 + a), Wx(I0 + k, J0 + bb), s);  // Z_II[a][k] = W[I0+k][I0+a]
-            Wx(J0 + bb, I0 + a) = dead[I0 + a] ? 0.f : -s;
+        // panel <- -T * Z_JJ
+        for (int i = t0 + warp; i < r; i += nwarps) {
+            if (lane < jb) {
+                float s = 0.f;
+                for (int k = lane; k < jb; ++k) s = fmaf(T[(size_t)(i - t0) * 32 + k], Lx(J + k, J + lane), s);
+                Lx(i, J + lane) = -s;
+            }
         }
+        (void)nt_rows;
         __syncthreads();
     }
-    for (int e = tid; e < r * r; e += nt) {
-        const int i = e / r, k = e % r;
-        if (k < i) Wx(i, k) = 0.f;
+    // W = L^{-1} row-major with a zero upper part; rows of dependent columns are zero,
+    // so the apply P <- P W^T leaves those columns of P at zero.
+    if (W) {
+        float* Wo = W + (size_t)b * rr;
+        for (int e = tid; e < r * r; e += nt) {
+            const int i = e / r, k = e % r;
+            Wo[e] = (k <= i && !deadsm[i]) ? Lx(i, k) : 0.f;
+        }
+    } else {
+        const size_t zs = (size_t)r * ldz;
+        bf16* z0 = Z3 + (size_t)3 * b * zs;
+        for (int e = tid; e < r * ldz; e += nt) {
+            const int i = e / ldz, k = e % ldz;
+            const float v = (k <= i && k < r && !deadsm[i]) ? Lx(i, k) : 0.f;
+            const bf16 h1 = __float2bfloat16_rn(v);
+            const float r1 = v - __bfloat162float(h1);
+            const bf16 h2 = __float2bfloat16_rn(r1);
+            const bf16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+            z0[e] = h1;
+            z0[zs + e] = h2;
+            z0[2 * zs + e] = h3;
+        }
     }
-#undef Wx
+#undef Lx0
 #undef Lx
     if (tid == 0 && s_bad) atomicOr(status, s_bad);
 }
 
-static cudaError_t chol_inv(int batch, int r, float* S, float* W, int* dead, int* status, cudaStream_t st)
+static size_t chol_smem_bytes(int r, bool in_smem)
 {
-    const size_t smem = ((size_t)r * (r + 1) + r) * sizeof(float);
-    if (smem <= 210 * 1024) {
+    const size_t scratch = (size_t)(r > 32 ? r - 32 : 0) * 32;
+    return in_smem ? ((size_t)r * (r + 1) + r + r + scratch) * sizeof(float) : (size_t)2 * r * sizeof(float);
+}
+
+cudaError_t chol_inv(int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
+                     int ldz, int* dead, int* status, cudaStream_t st)
+{
+    const size_t smem = chol_smem_bytes(r, true);
+    if (smem <= 225 * 1024) {
         static bool attr = false;
         if (!attr) {
             cudaError_t e = cudaFuncSetAttribute(chol_inv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 210 * 1024);
+                                                 225 * 1024);
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, S, W, dead,
-                      status);
+        return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, Sin, nparts, Swork,
+                      Wbuf, W, Z3, ldz, dead, status);
     }
-    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(512), (size_t)r * sizeof(float), st,
-                  r, S, W, dead, status);
+    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
+                  Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status);
 }
 
 cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,
@@ -206,10 +243,11 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
                                      LdB<float, true>{src, sp, ldp}, LdB<float, true>{src, sp, ldp},
                                      EpStore{S, ss, r}, st);
         if (e != cudaSuccess) return e;
-        e = chol_inv(batch, r, S, W, dead, status, st);
+        e = chol_inv(batch, r, S, 1, S, W, W, nullptr, 0, dead, status, st);
         if (e != cudaSuccess) return e;
-        e = gemm_simt<1>("qr_apply", batch, m, r, r, LdA<float, true>{src, sp, ldp}, LdB<float, true>{W, ss, r},
-                         LdB<float, true>{W, ss, r}, EpStore{dst, sp, ldp}, st);
+        // P <- P L^{-T}: B(k, j) = L^{-1}[j][k]
+        e = gemm_simt<1>("qr_apply", batch, m, r, r, LdA<float, true>{src, sp, ldp}, LdB<float, false>{W, ss, r},
+                         LdB<float, false>{W, ss, r}, EpStore{dst, sp, ldp}, st);
         if (e != cudaSuccess) return e;
         float* t = src; src = dst; dst = t;
     }

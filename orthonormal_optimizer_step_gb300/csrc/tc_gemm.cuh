@@ -27,6 +27,13 @@ struct TcGemmEpi {
     bf16* CT; long long ldct, sct;  // optional transposed copy of the output (N x M)
     float alpha, beta;
     int* status;
+    float* Cf;                      // if set: float32 output (row pitch ldc, matrix pitch sc) instead of C
+    // K segments: the contraction runs over nseg segments of K each; segment q
+    // reads operand matrices zmul*b + asel[q] (A) and zmul*b + bsel[q] (B),
+    // 4-bit entries packed in asel/bsel.  seg_batch = 1: each segment is its own
+    // output matrix (index nseg*b + q) instead of being accumulated.
+    int nseg, zmul, seg_batch;
+    uint32_t asel, bsel;
 };
 
 template <int BN>
@@ -59,6 +66,17 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
         } else {
             for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, __bfloat162float(ap[i]), acc[i]);
         }
+    }
+    if (ep.Cf) {
+        float* fp = ep.Cf + b * ep.sc + (long long)row * ep.ldc + col0;
+        if (ncol == 32 && (ep.ldc & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(fp + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        } else {
+            for (int i = 0; i < ncol; ++i) fp[i] = acc[i];
+        }
+        return;
     }
     bf16* cp = ep.C + b * ep.sc + (long long)row * ep.ldc + col0;
     if (ncol == 32) {
@@ -129,13 +147,19 @@ __global__ void __launch_bounds__(192, 1)
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
                 const int b = t / per_mat, rem = t % per_mat;
                 const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
-                for (int kc = 0; kc < kchunks; ++kc) {
-                    if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) break;
-                    uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
-                    tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                    tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, b);
-                    tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, b);
-                    if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                const int q0 = ep.seg_batch ? b % ep.nseg : 0, q1 = ep.seg_batch ? q0 + 1 : ep.nseg;
+                const int bm = ep.seg_batch ? b / ep.nseg : b;
+                for (int q = q0; q < q1; ++q) {
+                    const int za = bm * ep.zmul + (int)((ep.asel >> (4 * q)) & 15u);
+                    const int zb = bm * ep.zmul + (int)((ep.bsel >> (4 * q)) & 15u);
+                    for (int kc = 0; kc < kchunks; ++kc) {
+                        if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) break;
+                        uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+                        tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                        tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
+                        tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
+                        if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                    }
                 }
             }
         }
@@ -152,7 +176,8 @@ __global__ void __launch_bounds__(192, 1)
                 tc::tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
                 bool ok = true;
-                for (int kc = 0; kc < kchunks; ++kc) {
+                const int nchunks = kchunks * (ep.seg_batch ? 1 : ep.nseg);
+                for (int kc = 0; kc < nchunks; ++kc) {
                     if (!tc::mbar_wait(&full[stage], ph, abrt, ep.status)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(smem + stage * Cfg::STAGE_BYTES);
