@@ -4,6 +4,7 @@
 #include "common.cuh"
 
 namespace dion {
+namespace {   // internal linkage: one copy per translation unit
 
 // Momentum and Frobenius norms.  Block bh = (matrix b, head h) covers rows
 // [0, m) x columns [h*hd, (h+1)*hd).  If M != NULL: M <- mu M + G, y = M;
@@ -35,4 +36,5 @@ __global__ void __launch_bounds__(256) ns_prep_kernel(int m, int n, int hd, int 
     if (threadIdx.x == 0) atomicAdd(&nrm[bh], red[0]);
 }
 
+}  // namespace
 }  // namespace dion

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
                     const float piv = ok ? sqrtf(d) : 1.f;
                     if (lane == 0) {
                         dead[J + c] = !ok;
+                        deadsm[J + c] = !ok;
                         if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
                     }
                     const float lv = (lane > c) ? (ok ? a[c] / piv : 0.f) : (lane == c ? piv : a[c]);

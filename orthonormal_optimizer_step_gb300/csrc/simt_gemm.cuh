@@ -53,6 +53,10 @@ struct EpStore {
     }
 };
 
+// Kernels defined in this header get internal linkage (one copy per
+// translation unit).
+namespace {
+
 template <int NACC, class AL, class BL, class BL2, class EP>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(int Md, int Nd, int Kd, AL al, BL bl, BL2 bl2, EP ep)
 {
@@ -122,5 +126,7 @@ cudaError_t gemm_simt(const char* name, int batch, int Md, int Nd, int Kd, AL al
     dim3 grid((unsigned)cdiv(Nd, 64), (unsigned)cdiv(Md, 64), (unsigned)batch);
     return launch(name, gemm_simt_kernel<NACC, AL, BL, BL2, EP>, grid, dim3(256), 0, st, Md, Nd, Kd, al, bl, bl2, ep);
 }
+
+}  // namespace
 
 }  // namespace dion

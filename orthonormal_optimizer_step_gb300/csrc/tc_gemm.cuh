@@ -47,6 +47,12 @@ struct TcGemmCfg {
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
 };
 
+int num_sms();
+
+// Kernels defined in this header get internal linkage: every translation unit
+// that includes it owns its own copy (and its own one-time attribute setup).
+namespace {
+
 __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row, int col0, const uint32_t (&v)[32])
 {
     float acc[32];
@@ -224,8 +230,6 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-int num_sms();
-
 // Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN.
 template <int BN>
 cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
@@ -243,5 +247,7 @@ cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap&
     const int grid = tiles < num_sms() ? tiles : num_sms();
     return launch(name, tc_gemm_kernel<BN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
 }
+
+}  // namespace
 
 }  // namespace dion
