@@ -158,10 +158,32 @@ def run_gb300(args, rank, world, local_rank):
                                                            od.DION_BF16 if st["X"].dtype == torch.bfloat16
                                                            else od.DION_F32), dev)
 
+    # Shape groups are independent: each runs on its own stream, forked from
+    # and joined back to the timing stream every step.
+    main = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream() for _ in state] if args.group_streams else [main for _ in state]
+    fork = [torch.cuda.Event() for _ in state]
+    join = [torch.cuda.Event() for _ in state]
+
+    def grouped(fn):
+        for i, st in enumerate(state):
+            if streams[i] is not main:
+                fork[i].record(main)
+                streams[i].wait_event(fork[i])
+            with torch.cuda.stream(streams[i]):
+                fn(st, streams[i])
+            if streams[i] is not main:
+                join[i].record(streams[i])
+        for i in range(len(state)):
+            if streams[i] is not main:
+                main.wait_event(join[i])
+
+    def dion_one(st, s):
+        od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
+                             workspace=st["ws"], stream=s)
+
     def dion_step():
-        for st in state:
-            od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
-                                 workspace=st["ws"])
+        grouped(dion_one)
 
     def barrier():
         if world > 1:
@@ -231,10 +253,12 @@ def run_gb300(args, rank, world, local_rank):
                                                                 od.DION_BF16 if w.dtype == torch.bfloat16
                                                                 else od.DION_F32), dev)
 
+        def muon_one(st, s):
+            od.muon_ns_batched(st["G"], X=st["X"], M=st["Mn"], head_dim=st["g"].head_dim, steps=w.ns_steps,
+                               mu=w.mu, lr=w.lr, weight_decay=w.wd, workspace=st["wsn"], stream=s)
+
         def muon_step():
-            for st in state:
-                od.muon_ns_batched(st["G"], X=st["X"], M=st["Mn"], head_dim=st["g"].head_dim, steps=w.ns_steps,
-                                   mu=w.mu, lr=w.lr, weight_decay=w.wd, workspace=st["wsn"])
+            grouped(muon_one)
         msteps = max(1, args.steps // 2)
         for _ in range(max(1, args.warmup)):
             muon_step()
@@ -261,12 +285,17 @@ def run_gb300(args, rank, world, local_rank):
         h2d = sum(t.numel() * t.element_size() for t in hostG)
         d2h = sum(t.numel() * t.element_size() for t in hostX)
 
+        for st, hg, hx in zip(state, hostG, hostX):
+            st["hG"], st["hX"] = hg, hx
+
+        def e2e_one(st, s):
+            st["G"].copy_(st["hG"], non_blocking=True)
+            od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
+                                 workspace=st["ws"], stream=s)
+            st["hX"].copy_(st["X"], non_blocking=True)
+
         def e2e_step():
-            for st, hg, hx in zip(state, hostG, hostX):
-                st["G"].copy_(hg, non_blocking=True)
-                od.dion_step_batched(st["X"], st["G"], st["M"], st["Q"], mu=w.mu, lr=w.lr, weight_decay=w.wd,
-                                     workspace=st["ws"])
-                hx.copy_(st["X"], non_blocking=True)
+            grouped(e2e_one)
         for _ in range(2):
             e2e_step()
         esteps = max(1, args.steps // 2)
@@ -287,7 +316,8 @@ def run_gb300(args, rank, world, local_rank):
                 "config": {"workload": w.name, "groups": [[g.batch, g.m, g.n, g.rank(w.fraction)]
                                                           for g in w.groups],
                            "rank_fraction": w.fraction, "params": w.params,
-                           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                           "group_streams": len(state) if args.group_streams else 1},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clk, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
                 "muon": muon, "step_bytes": by, "step_flops": fl}
@@ -357,6 +387,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--one-stream", dest="group_streams", action="store_false",
+                    help="run the shape groups one after another on one stream")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "gb300" else args.warmup
 

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
 {
     extern __shared__ float smem[];
     __shared__ int s_bad;
+    __shared__ float s_emax;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
     const int nwarps = nt >> 5;
     const size_t rr = (size_t)r * r;
@@ -63,9 +64,50 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
     }
     __syncthreads();
     for (int i = tid; i < r; i += nt) d0[i] = Lx0(i);
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) { s_bad = 0; s_emax = 0.f; }
     __syncthreads();
 #define Lx(i, k) L[(size_t)(i) * ld + (k)]
+
+    // Near-identity Gram (the second CholeskyQR pass of a well-conditioned
+    // panel): S = I + E with max|E| <= 1e-4.  Then L = I + F with
+    // F = strictly_lower(E) + diag(E)/2 + O(E^2), and L^{-1} = I - F + O(E^2),
+    // so the factorization is skipped; the O(E^2) <= 1e-8 terms are below
+    // float32 rounding of the result.
+    {
+        float em = 0.f;
+        for (int e = tid; e < r * r; e += nt) {
+            const int i = e / r, k = e % r;
+            const float v = Lx(i, k) - (i == k ? 1.f : 0.f);
+            em = fmaxf(em, isfinite(v) ? fabsf(v) : 1e30f);
+        }
+        for (int o = 16; o > 0; o >>= 1) em = fmaxf(em, __shfl_xor_sync(0xffffffffu, em, o));
+        if (lane == 0) atomicMax((int*)&s_emax, __float_as_int(em));   // em >= 0: int order = float order
+        __syncthreads();
+        if (s_emax <= 1e-4f) {
+            for (int i = tid; i < r; i += nt) dead[i] = 0;
+            if (W) {
+                float* Wo = W + (size_t)b * rr;
+                for (int e = tid; e < r * r; e += nt) {
+                    const int i = e / r, k = e % r;
+                    Wo[e] = (k < i) ? -Lx(i, k) : (k == i ? 1.f - 0.5f * (Lx(i, i) - 1.f) : 0.f);
+                }
+            } else {
+                const size_t zs = (size_t)r * ldz;
+                bf16* z0 = Z3 + (size_t)3 * b * zs;
+                for (int e = tid; e < r * ldz; e += nt) {
+                    const int i = e / ldz, k = e % ldz;
+                    const float v = (k < i) ? -Lx(i, k) : (k == i ? 1.f - 0.5f * (Lx(i, i) - 1.f) : 0.f);
+                    const bf16 h1 = __float2bfloat16_rn(v);
+                    const float r1 = v - __bfloat162float(h1);
+                    const bf16 h2 = __float2bfloat16_rn(r1);
+                    z0[e] = h1;
+                    z0[zs + e] = h2;
+                    z0[2 * zs + e] = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+                }
+            }
+            return;
+        }
+    }
 
     for (int J = 0; J < r; J += 32) {
         const int jb = min(32, r - J);
