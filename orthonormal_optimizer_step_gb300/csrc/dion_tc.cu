@@ -66,6 +66,38 @@ __device__ __forceinline__ void load_b8(const float* M, const bf16* G, long long
     }
 }
 
+// Raw loads of 8 consecutive elements of M and G (issued early, converted later).
+struct Raw8 {
+    float4 a, c;
+    uint4 g;
+};
+
+template <bool VEC>
+__device__ __forceinline__ void fetch_b8(const float* M, const bf16* G, long long rowbase, int i, int m, int col, int n,
+                                         Raw8& r)
+{
+    if (VEC && i < m && col + 8 <= n) {
+        r.a = __ldg(reinterpret_cast<const float4*>(M + rowbase + col));
+        r.c = __ldg(reinterpret_cast<const float4*>(M + rowbase + col + 4));
+        r.g = __ldg(reinterpret_cast<const uint4*>(G + rowbase + col));
+    } else {
+        float v[8];
+        load_b8<false>(M, G, rowbase, i, m, col, n, v);   // already summed; G part set to zero
+        r.a = make_float4(v[0], v[1], v[2], v[3]);
+        r.c = make_float4(v[4], v[5], v[6], v[7]);
+        r.g = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+__device__ __forceinline__ uint4 sum_pack8(const Raw8& r)
+{
+    const bf16* h = reinterpret_cast<const bf16*>(&r.g);
+    float v[8] = {r.a.x + __bfloat162float(h[0]), r.a.y + __bfloat162float(h[1]), r.a.z + __bfloat162float(h[2]),
+                  r.a.w + __bfloat162float(h[3]), r.c.x + __bfloat162float(h[4]), r.c.y + __bfloat162float(h[5]),
+                  r.c.z + __bfloat162float(h[6]), r.c.w + __bfloat162float(h[7])};
+    return pack8(v);
+}
+
 struct PassArgs {
     int m, n, rp, batch;
     int rchunks;            // r-chunks of 256 columns
@@ -129,8 +161,33 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 8) {
-        // ---------------- producers: B = M + G -> bf16 -> swizzled A tile
+        // ---------------- producers: B = M + G -> bf16 -> swizzled A tile.
+        // The global loads of chunk kc + 1 are issued before chunk kc is
+        // converted and stored, so two chunks of loads are in flight.
+        Raw8 cur[4], nxt[4];
+        uint32_t off[4];
+        auto fetch = [&](int kc, Raw8 (&dst)[4]) {
+            const int k0 = (kc0 + kc) * kBK;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = threadIdx.x + kProducers * u;
+                if (!MN_A) {
+                    const int row = g >> 3, ch = g & 7;             // 128 rows x 8 chunks
+                    const int i = tile * kBM + row;
+                    fetch_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, k0 + ch * 8, a.n, dst[u]);
+                    off[u] = tc::sw128_offset(row, ch);
+                } else {
+                    const int row = g >> 4, ch = g & 15;            // 64 K-rows x 16 chunks
+                    const int i = k0 + row;
+                    fetch_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, tile * kBM + ch * 8, a.n,
+                                  dst[u]);
+                    off[u] = (ch >> 3) * 8192u + tc::sw128_offset(row, ch & 7);
+                }
+            }
+        };
+        if (nk > 0) fetch(0, cur);
         for (int kc = 0; kc < nk && !*abrt; ++kc) {
+            if (kc + 1 < nk) fetch(kc + 1, nxt);
             const int stage = kc % kStages;
             const uint32_t ph = (kc / kStages) & 1;
             if (lane == 0) tc::mbar_wait(&empty[stage], ph ^ 1, abrt, a.status);
@@ -148,25 +205,11 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int g = threadIdx.x + kProducers * u;
-                float v[8];
-                uint32_t off;
-                if (!MN_A) {
-                    const int row = g >> 3, ch = g & 7;             // 128 rows x 8 chunks
-                    const int i = tile * kBM + row;
-                    load_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, k0 + ch * 8, a.n, v);
-                    off = tc::sw128_offset(row, ch);
-                } else {
-                    const int row = g >> 4, ch = g & 15;            // 64 K-rows x 16 chunks
-                    const int i = k0 + row;
-                    load_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, tile * kBM + ch * 8, a.n, v);
-                    off = (ch >> 3) * 8192u + tc::sw128_offset(row, ch & 7);
-                }
-                *reinterpret_cast<uint4*>(sA + off) = pack8(v);
-            }
+            for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(sA + off[u]) = sum_pack8(cur[u]);
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(&full[stage]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
         }
     } else if (lane == 0) {
         // ---------------- MMA issuer
@@ -352,6 +395,191 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
     }
 }
 
+// ------------------------------------------------ persistent update pass
+// One CTA per SM walks the 128 x 64 tiles of M and X.  The M, G and X tiles
+// move between HBM and shared memory by TMA (two tile buffers, so the loads
+// of the next tile run under the math and the stores of this one), the P, R
+// and Q operands stream through two K stages, and the two accumulators
+// (P R^T, P Q^T) are double-buffered in tensor memory.
+//   warp 4: TMA producer     warp 5: MMA issuer     warps 0..3: epilogue
+struct UpdPArgs {
+    int m, n, batch, kchunks, tiles_m, tiles_n;
+    float one_minus_mu, decay, scale;
+    int* status;
+};
+
+constexpr uint32_t kPStage = kUStage;                              // 32 KB of operands per K chunk
+constexpr uint32_t kEM = 2 * 16384, kEG = 16384, kEX = 16384;      // M (two 32-column boxes), G, X
+constexpr uint32_t kEBuf = kEM + kEG + kEX;                        // 64 KB
+constexpr size_t kUpdPSmem = 2 * (size_t)kPStage + 2 * (size_t)kEBuf + 1024 + 256;
+
+__global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
+    const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmR,
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmM,
+    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX, UpdPArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* ops = smem;                              // [2][kPStage]
+    uint8_t* epi = smem + 2 * kPStage;                // [2][kEBuf]
+    uint64_t* ofull = (uint64_t*)(epi + 2 * kEBuf);
+    uint64_t* oempty = ofull + 2;
+    uint64_t* efull = oempty + 2;
+    uint64_t* eempty = efull + 2;
+    uint64_t* afull = eempty + 2;
+    uint64_t* aempty = afull + 2;
+    uint32_t* tmem_slot = (uint32_t*)(aempty + 2);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    volatile int* abrt = abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_mat = a.tiles_m * a.tiles_n, tiles = a.batch * per_mat;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&ofull[s], 1);
+            tc::mbar_init(&oempty[s], 1);
+            tc::mbar_init(&efull[s], 1);
+            tc::mbar_init(&eempty[s], 1);
+            tc::mbar_init(&afull[s], 1);
+            tc::mbar_init(&aempty[s], 4);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+                const int b = t / per_mat, rem = t % per_mat;
+                const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
+                const int eb = it & 1;
+                if (!tc::mbar_wait(&eempty[eb], ((it >> 1) & 1) ^ 1, abrt, a.status)) break;
+                uint8_t* e = epi + eb * kEBuf;
+                tc::mbar_arrive_expect_tx(&efull[eb], kEBuf);
+                tc::tma_load_3d(e, &tmM, &efull[eb], n0, m0, b);
+                tc::tma_load_3d(e + 16384, &tmM, &efull[eb], n0 + 32, m0, b);
+                tc::tma_load_3d(e + kEM, &tmG, &efull[eb], n0, m0, b);
+                tc::tma_load_3d(e + kEM + kEG, &tmX, &efull[eb], n0, m0, b);
+                for (int kc = 0; kc < a.kchunks; ++kc) {
+                    if (!tc::mbar_wait(&oempty[stage], ph ^ 1, abrt, a.status)) break;
+                    uint8_t* o = ops + stage * kPStage;
+                    tc::mbar_arrive_expect_tx(&ofull[stage], kPStage);
+                    tc::tma_load_3d(o, &tmP, &ofull[stage], kc * kBK, m0, b);
+                    tc::tma_load_3d(o + kUA, &tmR, &ofull[stage], kc * kBK, n0, b);
+                    tc::tma_load_3d(o + kUA + kUB, &tmQ, &ofull[stage], kc * kBK, n0, b);
+                    if (++stage == 2) { stage = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::make_idesc(kBM, kUBN, 1, false, false);
+            int stage = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+                const int ab = it & 1;
+                if (!tc::mbar_wait(&aempty[ab], ((it >> 1) & 1) ^ 1, abrt, a.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + ab * 128;
+                bool ok = true;
+                for (int kc = 0; kc < a.kchunks; ++kc) {
+                    if (!tc::mbar_wait(&ofull[stage], ph, abrt, a.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(ops + stage * kPStage), r0 = a0 + kUA, q0 = r0 + kUB;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
+                        tc::mma_bf16(d, ad, tc::make_sdesc(r0 + k * 32, 16, 1024), idesc, (kc | k) != 0);
+                        tc::mma_bf16(d + kUBN, ad, tc::make_sdesc(q0 + k * 32, 16, 1024), idesc, (kc | k) != 0);
+                    }
+                    tc::mma_commit(&oempty[stage]);
+                    if (++stage == 2) { stage = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(&afull[ab]);
+            }
+        }
+    } else {
+        const int row = warp * 32 + lane;            // tile row == TMEM lane
+        int it = 0;
+        for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+            const int b = t / per_mat, rem = t % per_mat;
+            const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
+            const int ab = it & 1, eb = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            const bool ok = tc::mbar_wait(&afull[ab], aph, abrt, a.status) &&
+                            tc::mbar_wait(&efull[eb], aph, abrt, a.status);
+            tc::tc_fence_after();
+            uint8_t* e = epi + eb * kEBuf;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {            // 32-column halves
+                uint32_t pr[32], pq[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ab * 128 + h * 32), pr);
+                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ab * 128 + kUBN + h * 32), pq);
+                tc::tmem_ld_wait();
+                if (!ok) continue;
+                uint8_t* eM = e + h * 16384;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {        // M: 8 chunks of 4 floats
+                    float4* pm = reinterpret_cast<float4*>(eM + tc::sw128_offset(row, c));
+                    const uint32_t gchunk = h * 4 + (c >> 1);
+                    const bf16* gh = reinterpret_cast<const bf16*>(e + kEM + tc::sw128_offset(row, gchunk)) + (c & 1) * 4;
+                    float4 mv = *pm;
+                    mv.x = mv.x + __bfloat162float(gh[0]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 0]);
+                    mv.y = mv.y + __bfloat162float(gh[1]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 1]);
+                    mv.z = mv.z + __bfloat162float(gh[2]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 2]);
+                    mv.w = mv.w + __bfloat162float(gh[3]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 3]);
+                    *pm = mv;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {        // X: 4 chunks of 8 bf16
+                    uint4* px = reinterpret_cast<uint4*>(e + kEM + kEG + tc::sw128_offset(row, h * 4 + c));
+                    uint4 xv = *px;
+                    const bf16* xh = reinterpret_cast<const bf16*>(&xv);
+                    float o[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        o[q] = a.decay * __bfloat162float(xh[q]) - a.scale * __uint_as_float(pq[8 * c + q]);
+                    *px = pack8(o);
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&aempty[ab]);
+            tc::fence_proxy_async_smem();
+            tc::named_bar_sync(1, 128);
+            if (threadIdx.x == 0) {
+                if (ok) {
+                    tc::tma_store_3d(&tmM, e, n0, m0, b);
+                    tc::tma_store_3d(&tmM, e + 16384, n0 + 32, m0, b);
+                    tc::tma_store_3d(&tmX, e + kEM + kEG, n0, m0, b);
+                    tc::tma_store_commit();
+                    tc::tma_store_wait_read();
+                }
+                tc::mbar_arrive(&eempty[eb]);
+            }
+        }
+        if (threadIdx.x == 0) tc::tma_store_wait_all();
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
 // ------------------------------------------------------------ small kernels
 
 // Qt[b][j][k] = bf16(Q[b][k][j]) for j < r; zero rows r <= j < rp.
@@ -534,7 +762,28 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         !make_tmap_3d(&tmR, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN) ||
         !make_tmap_3d(&tmQ, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN))
         return DION_ERR_CUDA;
-    {
+    if (vec) {
+        // persistent TMA-epilogue pass (needs 16-byte aligned rows of M, G, X)
+        CUtensorMap tmM, tmG, tmX;
+        const long long mn = (long long)m * n;
+        if (!make_tmap_3d(&tmM, M, TmapType::F32, n, m, batch, (long long)n * 4, mn * 4, 32, kBM) ||
+            !make_tmap_3d(&tmG, G, TmapType::BF16, n, m, batch, (long long)n * 2, mn * 2, 64, kBM) ||
+            !make_tmap_3d(&tmX, X, TmapType::BF16, n, m, batch, (long long)n * 2, mn * 2, 64, kBM))
+            return DION_ERR_CUDA;
+        static bool pattr = false;
+        if (!pattr) {
+            DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kUpdPSmem));
+            pattr = true;
+        }
+        const int tm = (int)cdiv(m, kBM), tn = (int)cdiv(n, kUBN);
+        const long long tiles = (long long)tm * tn * batch;
+        const int grid = (int)std::min<long long>(tiles, num_sms());
+        UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n),
+                    status};
+        DION_TRY(launch("dion_update_tc", dion_update_persist_kernel, dim3(grid), dim3(192), kUpdPSmem, st, tmPa, tmR,
+                        tmQ, tmM, tmG, tmX, ua));
+    } else {
         static bool attr[2] = {false, false};
         auto k = vec ? dion_update_tc_kernel<true> : dion_update_tc_kernel<false>;
         if (!attr[vec]) {
