@@ -212,16 +212,23 @@ def run_gb300(args, rank, world, local_rank):
     clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                     if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
 
-    # --- Dion (headline) ---
+    # --- Dion (headline): groups on their own streams, no per-kernel events
     for _ in range(args.warmup):
         dion_step()
     clocks.start()
-    prof = od.profile(max_launches=64 * args.steps * len(state) + 64)
-    ms = timed(dion_step, args.steps, prof)
-    torch.cuda.synchronize()
-    kernels = prof.read()
-    gpu_launches = sum(v[0] for v in kernels.values())
+    ms = timed(dion_step, args.steps)
     ms_step = ms / args.steps
+    # --- the same steps again, one group after another on one stream, with an
+    # event pair around every libdion kernel: per-kernel device times for the
+    # roofline (kernels of different groups do not share the GPU here)
+    saved_streams = list(streams)
+    streams[:] = [main for _ in state]
+    prof = od.profile(max_launches=64 * args.steps * len(state) + 64)
+    ms_seq = timed(dion_step, args.steps, prof) / args.steps
+    torch.cuda.synchronize()
+    streams[:] = saved_streams
+    kernels = prof.read()
+    gpu_launches = sum(v[0] for v in kernels.values())   # the headline region launches the same kernels
     by, fl = 0, 0.0
     eb = 2 if w.dtype == torch.bfloat16 else 4
     for st in state:
@@ -262,14 +269,18 @@ def run_gb300(args, rank, world, local_rank):
         msteps = max(1, args.steps // 2)
         for _ in range(max(1, args.warmup)):
             muon_step()
+        mms = timed(muon_step, msteps) / msteps
+        saved_streams = list(streams)
+        streams[:] = [main for _ in state]
         mprof = od.profile(max_launches=64 * msteps * len(state) * (w.ns_steps + 2))
-        mms = timed(muon_step, msteps, mprof) / msteps
+        mms_seq = timed(muon_step, msteps, mprof) / msteps
+        streams[:] = saved_streams
         mk = mprof.read()
         nfl = sum(ns_flops(st["g"], w.ns_steps) for st in state)
         gemm_ms = sum(v[1] for k, v in mk.items() if k.startswith("ns_") and ("gram" in k or "poly" in k
                                                                               or "axpy" in k))
         ach = nfl / (gemm_ms / msteps * 1e-3) / 1e12 if gemm_ms > 0 else None
-        muon = {"ms_per_step": mms, "tflops_step": nfl / (mms * 1e-3) / 1e12,
+        muon = {"ms_per_step": mms, "ms_per_step_one_stream": mms_seq, "tflops_step": nfl / (mms * 1e-3) / 1e12,
                 "roofline": {"bound": "tensor", "kernel": "ns gemm chain", "achieved": ach,
                              "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,
@@ -320,7 +331,8 @@ def run_gb300(args, rank, world, local_rank):
                            "group_streams": len(state) if args.group_streams else 1},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clk, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
-                "muon": muon, "step_bytes": by, "step_flops": fl}
+                "muon": muon, "step_bytes": by, "step_flops": fl, "ms_per_step_one_stream": ms_seq,
+                "kernels_note": "per-kernel times from a one-stream pass of the same steps"}
         print(json.dumps(line), flush=True)
 
 
