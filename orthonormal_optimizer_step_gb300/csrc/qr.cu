@@ -37,7 +37,7 @@ namespace dion {
 // (W != NULL), or as three bf16 terms Z3[3b + t] (pitch ldz, columns up to ldz,
 // Z = Z3[0] + Z3[1] + Z3[2] to float32 accuracy) for the tensor-core apply.
 template <bool kSmem>
-__global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
+__global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
                                                        float* W, bf16* Z3, int ldz, int* dead_g, int* status)
 {
     extern __shared__ float smem[];
@@ -54,13 +54,17 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
     float* L = kSmem ? smem : Sg;
     float* d0 = kSmem ? smem + (size_t)r * ld : smem;     // original diagonal
     int* deadsm = (int*)(d0 + r);                          // dependent-column flags
+    float* rinv_all = (float*)(deadsm + r);                // reciprocal pivots 1 / L(j, j) (0 if dependent)
 #define Lx0(i) (kSmem ? L[(size_t)(i) * ld + (i)] : Sg[(size_t)(i) * r + (i)])
-    float* T = kSmem ? (float*)(deadsm + r) : Wg;         // (r - 32) x 32 scratch of the inverse
-    for (int e = tid; e < r * r; e += nt) {
-        float v = Sb[e];
-        for (int q = 1; q < nparts; ++q) v += Sb[(size_t)q * rr + e];
-        if (kSmem) L[(size_t)(e / r) * ld + (e % r)] = v;
-        else Sg[e] = v;
+    float* T = kSmem ? rinv_all + r : Wg;                  // (r - 32) x 32 scratch of the inverse
+    for (int i = warp; i < r; i += nwarps) {
+        for (int k = lane; k < r; k += 32) {
+            const size_t e = (size_t)i * r + k;
+            float v = Sb[e];
+            for (int q = 1; q < nparts; ++q) v += Sb[(size_t)q * rr + e];
+            if (kSmem) L[(size_t)i * ld + k] = v;
+            else Sg[e] = v;
+        }
     }
     __syncthreads();
     for (int i = tid; i < r; i += nt) d0[i] = Lx0(i);
@@ -109,41 +113,43 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
         }
     }
 
+    // The loops below are kept rolled (modest unrolling only): the factorization
+    // is a long chain of short dependent steps, and compact code keeps them in
+    // the instruction cache.
     for (int J = 0; J < r; J += 32) {
         const int jb = min(32, r - J);
         if (warp == 0) {
-            // diagonal block in registers: lane = row, a[k] = L(J + lane, J + k)
-            float a[32];
+            // Diagonal block, lane = row.  w[j] holds L(J + lane, J + c + j):
+            // the current column is always w[0], and the window shifts by one
+            // column per step, so every register index is a compile-time
+            // constant inside a rolled loop.
+            float w[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) a[k] = (lane < jb && k < jb) ? Lx(J + lane, J + k) : 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                if (c < jb) {
-                    const float d = __shfl_sync(0xffffffffu, a[c], c);
-                    const bool fin = isfinite(d);
-                    const bool ok = fin && d > 1e-6f * d0[J + c];
-                    const float piv = ok ? sqrtf(d) : 1.f;
-                    if (lane == 0) {
-                        dead[J + c] = !ok;
-                        deadsm[J + c] = !ok;
-                        if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
-                    }
-                    const float lv = (lane > c) ? (ok ? a[c] / piv : 0.f) : (lane == c ? piv : a[c]);
-                    a[c] = lv;
-#pragma unroll
-                    for (int k = c + 1; k < 32; ++k) {
-                        const float lkc = __shfl_sync(0xffffffffu, lv, k);     // L(J + k, J + c)
-                        if (lane >= k && lane > c) a[k] = fmaf(-lv, lkc, a[k]);
-                    }
+            for (int j = 0; j < 32; ++j) w[j] = (lane < jb && j < jb) ? Lx(J + lane, J + j) : 0.f;
+            for (int c = 0; c < jb; ++c) {
+                const float d = __shfl_sync(0xffffffffu, w[0], c);
+                const bool fin = isfinite(d);
+                const bool ok = fin && d > 1e-6f * d0[J + c];
+                const float rinv = ok ? rsqrtf(d) : 0.f;
+                const float lv = (lane > c) ? w[0] * rinv : (lane == c ? (ok ? d * rinv : 1.f) : 0.f);
+                if (lane == 0) {
+                    deadsm[J + c] = !ok;
+                    rinv_all[J + c] = rinv;
+                    if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
                 }
-            }
-            if (lane < jb)
+                if (lane >= c && lane < jb) Lx(J + lane, J + c) = lv;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (k < jb) Lx(J + lane, J + k) = a[k];
+                for (int j = 1; j < 32; ++j) {
+                    const float lk = __shfl_sync(0xffffffffu, lv, (c + j) & 31);   // L(J + c + j, J + c)
+                    if (lane > c && lane >= c + j) w[j] = fmaf(-lv, lk, w[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 31; ++j) w[j] = w[j + 1];
+                w[31] = 0.f;
+            }
         }
         __syncthreads();
-        // panel below the diagonal block: one thread per row, row held in registers
+        // panel below the diagonal block: one thread per row, x L_JJ^T = row
         for (int i = J + jb + tid; i < r; i += nt) {
             float a[32];
 #pragma unroll
@@ -151,10 +157,13 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 if (c < jb) {
-                    float s = a[c];
+                    float lr[32];
 #pragma unroll
-                    for (int k = 0; k < c; ++k) s = fmaf(-a[k], Lx(J + c, J + k), s);
-                    a[c] = deadsm[J + c] ? 0.f : s / Lx(J + c, J + c);
+                    for (int k = 0; k < c; ++k) lr[k] = Lx(J + c, J + k);
+                    float s4[4] = {a[c], 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < c; ++k) s4[k & 3] = fmaf(-a[k], lr[k], s4[k & 3]);
+                    a[c] = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * rinv_all[J + c];
                 }
             }
 #pragma unroll
@@ -165,63 +174,96 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
         // trailing lower triangle: one warp per row i, lanes over k
         const int t0 = J + jb;
         for (int i = t0 + warp; i < r; i += nwarps) {
-            float li[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) li[c] = (c < jb) ? Lx(i, J + c) : 0.f;
+            const float* li = &Lx(i, J);
             for (int k = t0 + lane; k <= i; k += 32) {
-                float s = 0.f;
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c < jb) s = fmaf(li[c], Lx(k, J + c), s);
-                Lx(i, k) -= s;
+                const float* lk = &Lx(k, J);
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                int c = 0;
+                for (; c + 3 < jb; c += 4) {
+                    s4[0] = fmaf(li[c], lk[c], s4[0]);
+                    s4[1] = fmaf(li[c + 1], lk[c + 1], s4[1]);
+                    s4[2] = fmaf(li[c + 2], lk[c + 2], s4[2]);
+                    s4[3] = fmaf(li[c + 3], lk[c + 3], s4[3]);
+                }
+                for (; c < jb; ++c) s4[0] = fmaf(li[c], lk[c], s4[0]);
+                Lx(i, k) -= (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
         }
         __syncthreads();
     }
 
+    // ---- diagonal blocks Z_II = L_II^{-1}, all at once (one warp per block):
+    // lane c computes column c right-looking; acc[j] is the partial right-hand
+    // side of row i + j.
+    for (int I = warp; I * 32 < r; I += nwarps) {
+        const int J = I * 32, jb = min(32, r - J), c = lane;
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = (j == c) ? 1.f : 0.f;
+        float zc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            zc[i] = 0.f;
+            if (i < jb) {
+                const float z = (i >= c && c < jb) ? acc[0] * rinv_all[J + i] : 0.f;
+                zc[i] = z;
+#pragma unroll
+                for (int j = 1; j < 32; ++j) {
+                    const float l = Lx(J + min(i + j, jb - 1), J + i);
+                    acc[j] = (i + j < jb) ? fmaf(-l, z, acc[j]) : acc[j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 31; ++j) acc[j] = acc[j + 1];
+            acc[31] = 0.f;
+        }
+        __syncwarp();
+        if (c < jb)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i >= c && i < jb) Lx(J + i, J + c) = zc[i];
+    }
+    __syncthreads();
+
     // ---- in-place inverse L <- L^{-1}, block columns from the last one back:
     //   Z_JJ = L_JJ^{-1};  panel <- -(L^{-1} of the trailing part) * panel * Z_JJ
     for (int J = ((r - 1) / 32) * 32; J >= 0; J -= 32) {
-        const int jb = min(32, r - J), t0 = J + jb, nt_rows = r - t0;
+        const int jb = min(32, r - J), t0 = J + jb;
         // T = Linv_trail * panel  (rows t0..r-1, 32 columns), one warp per row
         for (int i = t0 + warp; i < r; i += nwarps) {
-            float s = 0.f;
-            if (lane < jb)
-                for (int k = t0; k <= i; ++k) s = fmaf(Lx(i, k), Lx(k, J + lane), s);
-            T[(size_t)(i - t0) * 32 + lane] = s;
-        }
-        if (warp == 0) {
-            // Z_JJ: lane c computes column c by forward substitution (registers)
-            const int c = lane;
-            float z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float v = (i == c) ? 1.f : 0.f;
-                if (i < jb) {
-#pragma unroll
-                    for (int k = 0; k < i; ++k)
-                        if (k >= c) v = fmaf(-Lx(J + i, J + k), z[k], v);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            if (lane < jb) {
+                int k = t0;
+                for (; k + 3 <= i; k += 4) {
+                    s0 = fmaf(Lx(i, k), Lx(k, J + lane), s0);
+                    s1 = fmaf(Lx(i, k + 1), Lx(k + 1, J + lane), s1);
+                    s2 = fmaf(Lx(i, k + 2), Lx(k + 2, J + lane), s2);
+                    s3 = fmaf(Lx(i, k + 3), Lx(k + 3, J + lane), s3);
                 }
-                z[i] = (i >= c && i < jb && c < jb) ? v / Lx(J + i, J + i) : 0.f;
+                for (; k <= i; ++k) s0 = fmaf(Lx(i, k), Lx(k, J + lane), s0);
             }
-            __syncwarp();
-            if (c < jb)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i >= c && i < jb) Lx(J + i, J + c) = z[i];
+            T[(size_t)(i - t0) * 32 + lane] = (s0 + s1) + (s2 + s3);
         }
         __syncthreads();
         // panel <- -T * Z_JJ
         for (int i = t0 + warp; i < r; i += nwarps) {
             if (lane < jb) {
-                float s = 0.f;
-                for (int k = lane; k < jb; ++k) s = fmaf(T[(size_t)(i - t0) * 32 + k], Lx(J + k, J + lane), s);
-                Lx(i, J + lane) = -s;
+                const float* Ti = T + (size_t)(i - t0) * 32;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                int k = lane;
+                for (; k + 3 < jb; k += 4) {
+                    s4[0] = fmaf(Ti[k], Lx(J + k, J + lane), s4[0]);
+                    s4[1] = fmaf(Ti[k + 1], Lx(J + k + 1, J + lane), s4[1]);
+                    s4[2] = fmaf(Ti[k + 2], Lx(J + k + 2, J + lane), s4[2]);
+                    s4[3] = fmaf(Ti[k + 3], Lx(J + k + 3, J + lane), s4[3]);
+                }
+                for (; k < jb; ++k) s4[0] = fmaf(Ti[k], Lx(J + k, J + lane), s4[0]);
+                Lx(i, J + lane) = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
             }
         }
-        (void)nt_rows;
         __syncthreads();
     }
+    for (int i = tid; i < r; i += nt) dead[i] = deadsm[i];
     // W = L^{-1} row-major with a zero upper part; rows of dependent columns are zero,
     // so the apply P <- P W^T leaves those columns of P at zero.
     if (W) {
@@ -253,18 +295,18 @@ __global__ void __launch_bounds__(512) chol_inv_kernel(int r, const float* Sin, 
 static size_t chol_smem_bytes(int r, bool in_smem)
 {
     const size_t scratch = (size_t)(r > 32 ? r - 32 : 0) * 32;
-    return in_smem ? ((size_t)r * (r + 1) + r + r + scratch) * sizeof(float) : (size_t)2 * r * sizeof(float);
+    return in_smem ? ((size_t)r * (r + 1) + 3 * (size_t)r + scratch) * sizeof(float) : (size_t)3 * r * sizeof(float);
 }
 
 cudaError_t chol_inv(int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
                      int ldz, int* dead, int* status, cudaStream_t st)
 {
     const size_t smem = chol_smem_bytes(r, true);
-    if (smem <= 225 * 1024) {
+    if (smem <= 215 * 1024) {
         static bool attr = false;
         if (!attr) {
             cudaError_t e = cudaFuncSetAttribute(chol_inv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 225 * 1024);
+                                                 215 * 1024);
             if (e != cudaSuccess) return e;
             attr = true;
         }
