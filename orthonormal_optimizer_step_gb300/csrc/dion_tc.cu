@@ -6,15 +6,14 @@
 //   2. dion_bq_tc    : P = B Q with B = M + G formed in registers, rounded to
 //                      bf16 and written straight into the swizzled MMA operand
 //                      tile (B is never stored); split over n, fp32 partials
-//   3. dion_reduce   : P = sum of partials
-//   4. CholeskyQR2 of P (float32 accuracy; products on the tensor cores,
-//      qr_tc.cu)
-//   5. dion_prep_p   : P16 = bf16(P)
+//   3-5. CholeskyQR2 of P (float32 accuracy; products on the tensor cores,
+//      qr_tc.cu): its first pass reads the partials, its last product also
+//      writes P16 = bf16(P)
 //   6. dion_btp_tc   : R = B^T P, contracting over m: both operands are read
 //                      MN-major (B rows are K rows), so B is again formed in
 //                      registers without any transpose; split over m
-//   7. dion_reduce   : R = sum of partials; column norms; Q = R / ||R_j||
-//   8. dion_prep_rq  : R16 = bf16(R), Q16 = bf16(Q)
+//   7. dion_rsum     : R = sum of partials, R16 = bf16(R), partial column norms
+//   8. dion_norm_final, dion_qemit: Q = R / ||R_j|| (caller's fp32 Q) and Q16
 //   9. dion_update_tc: per 128 x 64 tile, two accumulators P R^T and P Q^T in
 //                      tensor memory; the epilogue streams M, G, X once:
 //                      M <- M + G - (1-mu) P R^T,  X <- (1-lr wd) X - lr sqrt(m/n) P Q^T
@@ -599,35 +598,65 @@ __global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp,
     }
 }
 
-// dst[e] = sum_s part[s][e] over `count` floats (count % 4 == 0).
-__global__ void __launch_bounds__(256) dion_reduce_kernel(long long count, int splits, const float* part, float* dst)
+// R = sum of the split partials (fp32, pitch rp), R16 = bf16(R) (columns r..rp-1
+// zero), and per-chunk column sums of squares normpart[b][chunk][c] over rows
+// chunk*kRChunk ..: every sum in a fixed order, so results are reproducible.
+constexpr int kRChunk = 32;
+
+__global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, int splits, int batch,
+                                                        const float* __restrict__ part, float* __restrict__ R,
+                                                        bf16* __restrict__ R16, float* __restrict__ normpart)
 {
-    const long long n4 = count / 4;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += (long long)gridDim.x * blockDim.x) {
-        float4 s = reinterpret_cast<const float4*>(part)[e];
-        for (int k = 1; k < splits; ++k) {
-            const float4 t = reinterpret_cast<const float4*>(part + (long long)k * count)[e];
-            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+    const int b = blockIdx.y, chunk = blockIdx.x, nchunks = gridDim.x;
+    const int j0 = chunk * kRChunk, j1 = min(n, j0 + kRChunk);
+    const long long pstride = (long long)batch * n * rp;
+    for (int c = threadIdx.x; c < rp; c += blockDim.x) {
+        float ss = 0.f;
+#pragma unroll 4
+        for (int j = j0; j < j1; ++j) {
+            const long long o = ((long long)b * n + j) * rp + c;
+            float v = part[o];
+            for (int q = 1; q < splits; ++q) v += part[o + q * pstride];
+            if (c >= r) v = 0.f;
+            R[o] = v;
+            R16[o] = __float2bfloat16_rn(v);
+            ss = fmaf(v, v, ss);
         }
-        reinterpret_cast<float4*>(dst)[e] = s;
+        normpart[((long long)b * nchunks + chunk) * rp + c] = ss;
     }
 }
 
-// dst = bf16(src) over rows x rp, with columns c >= r set to zero.  If inv is
-// given, column c is scaled by inv[b*r + c] (Q16 = bf16(R / ||R_c||)).
-__global__ void __launch_bounds__(256) dion_to_bf16_kernel(long long rows_total, int rows, int r, int rp,
-                                                           const float* src, const float* inv, bf16* dst)
+// inv[b][c] = 1 / max(||R_c||, floor) for c < r, 0 for the padding columns.
+__global__ void __launch_bounds__(256) dion_norm_final_kernel(int r, int rp, int nchunks,
+                                                              const float* __restrict__ normpart, float* inv,
+                                                              float floor_nrm, int* status)
 {
-    const long long total = rows_total * rp;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-        const int c = (int)(e % rp);
-        const long long row = e / rp;
+    const int b = blockIdx.x;
+    for (int c = threadIdx.x; c < rp; c += blockDim.x) {
+        float t = 0.f;
+        for (int k = 0; k < nchunks; ++k) t += normpart[((long long)b * nchunks + k) * rp + c];
         float v = 0.f;
         if (c < r) {
-            v = src[e];
-            if (inv) v *= inv[(row / rows) * r + c];
+            v = 1.f / fmaxf(sqrtf(t), floor_nrm);
+            if (!isfinite(t)) atomicOr(status, kStatusNonFinite);
         }
-        dst[e] = __float2bfloat16_rn(v);
+        inv[(long long)b * rp + c] = v;
+    }
+}
+
+// Q = R * inv (the caller's n x r float32 state) and Q16 = bf16(Q) (n x rp operand).
+__global__ void __launch_bounds__(256) dion_qemit_kernel(int n, int r, int rp, long long total,
+                                                         const float* __restrict__ R, const float* __restrict__ inv,
+                                                         float* __restrict__ Q, bf16* __restrict__ Q16)
+{
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % rp);
+        const long long row = e / rp;                 // b * n + j
+        const int b = (int)(row / n);
+        const float q = R[e] * inv[(long long)b * rp + c];
+        Q16[e] = __float2bfloat16_rn(q);
+        if (c < r) Q[row * r + c] = q;
     }
 }
 
@@ -705,6 +734,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     bf16* P16 = (bf16*)(ws + L.P16);
     bf16* R16 = (bf16*)(ws + L.R16);
     bf16* Q16 = (bf16*)(ws + L.Q16);
+    float* normp = (float*)(ws + L.normp);
     const long long np = (long long)align_up((size_t)n, 8);
     const bool vec = (n % 8) == 0;
     const int rchunks = (int)cdiv(rp, 256);
@@ -724,15 +754,10 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
         DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, dim3((unsigned)cdiv(m, kBM), splits * rchunks, batch),
                                     pa, st));
-        const long long cnt = (long long)batch * m * rp;
-        DION_TRY(launch("dion_reduce_p", dion_reduce_kernel, dim3(grid_for(cnt / 4)), dim3(256), 0, st, cnt, splits,
-                        (const float*)part, P0));
+        // 3-5. CholeskyQR2; its first pass reads the split partials of P directly, its
+        // last product writes P (float32, P0) and P16 = bf16(P)
+        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st));
     }
-    // 4. CholeskyQR2 on P (first r columns; padded columns stay zero)
-    DION_TRY(qr_cholesky2_tc(batch, m, r, rp, P0, P1, ws, L, status, st));
-    // 5. P16 = bf16(P)
-    DION_TRY(launch("dion_prep_p", dion_to_bf16_kernel, dim3(grid_for((long long)batch * m * rp)), dim3(256), 0, st,
-                    (long long)batch * m, m, r, rp, (const float*)P0, (const float*)nullptr, P16));
     // 6. R partials = B^T P
     CUtensorMap tmP64;
     if (!make_tmap_3d(&tmP64, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
@@ -744,18 +769,19 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
         DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, dim3((unsigned)cdiv(n, kBM), splits * rchunks, batch),
                                    pa, st));
-        const long long cnt = (long long)batch * n * rp;
-        DION_TRY(launch("dion_reduce_r", dion_reduce_kernel, dim3(grid_for(cnt / 4)), dim3(256), 0, st, cnt, splits,
-                        (const float*)part, R));
+        // 7. R = sum of partials, R16, column norms, Q = R / ||R_j||, Q16
+        const int nchunks = (int)cdiv(n, kRChunk);
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp,
+                        splits, batch, (const float*)part, R, R16, normp));
     }
-    // 7. Q = R / ||R_j||
-    DION_TRY(launch("dion_colnorm", dion_colnorm_tc_kernel, dim3((unsigned)cdiv(r, 32), batch), dim3(32, 8), 0, st, n,
-                    r, (long long)rp, (const float*)R, Q, inv, 1e-12f * sqrtf((float)n), status));
-    // 8. R16, Q16
-    DION_TRY(launch("dion_prep_r", dion_to_bf16_kernel, dim3(grid_for((long long)batch * n * rp)), dim3(256), 0, st,
-                    (long long)batch * n, n, r, rp, (const float*)R, (const float*)nullptr, R16));
-    DION_TRY(launch("dion_prep_q", dion_to_bf16_kernel, dim3(grid_for((long long)batch * n * rp)), dim3(256), 0, st,
-                    (long long)batch * n, n, r, rp, (const float*)R, (const float*)inv, Q16));
+    {
+        const int nchunks = (int)cdiv(n, kRChunk);
+        DION_TRY(launch("dion_norm_final", dion_norm_final_kernel, dim3(batch), dim3(256), 0, st, r, rp, nchunks,
+                        (const float*)normp, inv, 1e-12f * sqrtf((float)n), status));
+        const long long total = (long long)batch * n * rp;
+        DION_TRY(launch("dion_qemit", dion_qemit_kernel, dim3(grid_for(total)), dim3(256), 0, st, n, r, rp, total,
+                        (const float*)R, (const float*)inv, Q, Q16));
+    }
     // 9. M and X updates
     CUtensorMap tmPa, tmR, tmQ;
     if (!make_tmap_3d(&tmPa, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||

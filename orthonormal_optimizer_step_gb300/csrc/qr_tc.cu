@@ -32,7 +32,9 @@ __device__ __forceinline__ void split3(float v, bf16& h1, bf16& h2, bf16& h3)
 
 // P (m x rp fp32, pitch rp) -> P3[3b + t] (m x rp, natural) and T3[3b + t]
 // (rp x mp, transposed), t = 0, 1, 2 the three bf16 terms.
-__global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, const float* P, bf16* P3, bf16* T3)
+// P may be given as nparts split partials (summed here, pitch pstride).
+__global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, const float* P, int nparts,
+                                                       long long pstride, bf16* P3, bf16* T3)
 {
     __shared__ float tile[32][33];
     const int b = blockIdx.z, c0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
@@ -41,13 +43,15 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, co
         const int i = i0 + ii, c = c0 + threadIdx.x;
         float v = 0.f;
         if (i < m && c < rp) {
-            v = P[(size_t)b * pn + (size_t)i * rp + c];
+            const size_t o = (size_t)b * pn + (size_t)i * rp + c;
+            v = P[o];
+            for (int q = 1; q < nparts; ++q) v += P[o + q * pstride];
             bf16 h1, h2, h3;
             split3(v, h1, h2, h3);
-            bf16* o = P3 + (size_t)3 * b * pn + (size_t)i * rp + c;
-            o[0] = h1;
-            o[pn] = h2;
-            o[2 * pn] = h3;
+            bf16* po = P3 + (size_t)3 * b * pn + (size_t)i * rp + c;
+            po[0] = h1;
+            po[pn] = h2;
+            po[2 * pn] = h3;
         }
         tile[ii][threadIdx.x] = v;
     }
@@ -77,8 +81,8 @@ cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUte
 
 }  // namespace
 
-cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* P, float* Ptmp, char* ws, const DionLayout& L,
-                            int* status, cudaStream_t st)
+cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
+                            bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st)
 {
     bf16* T3 = (bf16*)(ws + L.T3);
     bf16* P3 = (bf16*)(ws + L.P3);
@@ -97,11 +101,13 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* P, float* Pt
         !make_tmap_3d(&tZb, Z3, TmapType::BF16, rp, r, 3ll * batch, (long long)rp * 2, (long long)r * rp * 2, 64, bna))
         return cudaErrorInvalidValue;
 
-    float* src = P;
-    float* dst = Ptmp;
+    // pass 1: split partials of P -> Ptmp;  pass 2: Ptmp -> P (and P16)
     for (int pass = 0; pass < 2; ++pass) {
+        const float* src = pass == 0 ? Pin : Ptmp;
+        float* dst = pass == 0 ? Ptmp : P;
+        const int np_ = pass == 0 ? nparts : 1;
         cudaError_t e = launch("qr_split", qr_split_kernel, dim3((unsigned)cdiv(rp, 32), (unsigned)cdiv(m, 32), batch),
-                               dim3(32, 8), 0, st, m, rp, (int)mp, (const float*)src, P3, T3);
+                               dim3(32, 8), 0, st, m, rp, (int)mp, src, np_, (long long)batch * m * rp, P3, T3);
         if (e != cudaSuccess) return e;
         // six partial Grams S6[6b + q] = T_a(q) T_b(q)^T  (r x r)
         TcGemmEpi eg{r, r, (int)cdiv(r, 128), (int)cdiv(r, bn), 6 * batch, nullptr, r, (long long)r * r,
@@ -111,11 +117,10 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* P, float* Pt
         e = chol_inv(batch, r, S6, 6, S, W, nullptr, Z3, rp, dead, status, st);
         if (e != cudaSuccess) return e;
         // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
-        TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, nullptr, rp, (long long)m * rp,
-                     nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, dst, 6, 3, 0, kSelA, kSelB};
+        TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
+                     (long long)m * rp, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, dst, 6, 3, 0, kSelA, kSelB};
         e = gemm_any(bna, "qr_apply_tc", tPa, tZb, rp, ea, st);
         if (e != cudaSuccess) return e;
-        float* t = src; src = dst; dst = t;
     }
     return cudaSuccess;
 }

@@ -27,7 +27,8 @@ struct TcGemmEpi {
     bf16* CT; long long ldct, sct;  // optional transposed copy of the output (N x M)
     float alpha, beta;
     int* status;
-    float* Cf;                      // if set: float32 output (row pitch ldc, matrix pitch sc) instead of C
+    float* Cf;                      // if set: float32 output (row pitch ldc, matrix pitch sc); C, if also
+                                    // set, receives a bf16 copy
     // K segments: the contraction runs over nseg segments of K each; segment q
     // reads operand matrices zmul*b + asel[q] (A) and zmul*b + bsel[q] (B),
     // 4-bit entries packed in asel/bsel.  seg_batch = 1: each segment is its own
@@ -82,7 +83,7 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
         } else {
             for (int i = 0; i < ncol; ++i) fp[i] = acc[i];
         }
-        return;
+        if (!ep.C) return;             // else also a bf16 copy with the same pitches
     }
     bf16* cp = ep.C + b * ep.sc + (long long)row * ep.ldc + col0;
     if (ncol == 32) {
