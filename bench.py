@@ -120,24 +120,36 @@ def ns_flops(g, steps):
     return g.batch * heads * steps * (4.0 * s * s * l + 2.0 * s ** 3)
 
 
-# per-kernel algorithmic bytes for the roofline of the dominant Dion kernel
-def kernel_bytes(name, w, state):
+# Algorithmic cost of one step's launches of a kernel, summed over the shape
+# groups: ("hbm", bytes) for the streaming passes, ("alu", fp32 flops) for the
+# r x r factorization, ("tensor", flops) for the QR products.
+def kernel_cost(name, w, state):
     eb = 2 if str(w.dtype).endswith("bfloat16") else 4
-    tot = 0
+    tot, bound = 0.0, "hbm"
     for st in state:
         g, r = st["g"], st["r"]
+        rp = -(-r // 64) * 64
         mn = g.batch * g.m * g.n
         if name.startswith("dion_bq"):
-            tot += mn * (4 + eb) + g.batch * (g.n * r * 4 + g.m * r * 4)
+            tot += mn * (4 + eb) + g.batch * (g.n * r * 2 + g.m * rp * 4)
         elif name.startswith("dion_btp"):
-            tot += mn * (4 + eb) + g.batch * (g.m * r * 4 + g.n * r * 4)
+            tot += mn * (4 + eb) + g.batch * (g.m * rp * 2 + g.n * rp * 4)
         elif name.startswith("dion_update"):
-            tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * r * 4 + 2 * g.n * r * 4)
-        elif name.startswith("dion_fused"):
-            tot += mn * (4 + eb + 4) + g.batch * (g.m * r * 4 + g.n * r * 4)
-        elif name.startswith("dion_xupd"):
-            tot += mn * (2 * eb) + g.batch * (g.m * r * 4 + g.n * r * 4)
-    return tot
+            tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * rp * 2 + 2 * g.n * rp * 2)
+        elif name.startswith("chol_inv_pass1"):
+            bound = "alu"
+            tot += g.batch * (2.0 / 3.0) * r ** 3          # Cholesky r^3/3 + triangular inverse r^3/3
+        elif name.startswith("qr_gram") or name.startswith("qr_apply"):
+            bound = "tensor"
+            tot += g.batch * 6 * 2.0 * g.m * r * r          # six bf16 cross-term products
+        else:
+            return None, 0.0
+    return bound, tot
+
+
+def alu_peak_tflops(sm_mhz=2070.0, sms=152):
+    """fp32 FMA peak: SMs x 128 lanes x 2 flops x clock."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ----------------------------------------------------------------- arms
@@ -238,13 +250,28 @@ def run_gb300(args, rank, world, local_rank):
     # dominant kernel by device time
     dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else (None, (0, 0.0))
     dom_name, (dom_launches, dom_ms) = dom
-    dom_bytes = kernel_bytes(dom_name or "", w, state) / max(1, len(state))
+    bound, cost_step = kernel_cost(dom_name or "", w, state)
     per_launch_ms = dom_ms / max(dom_launches, 1)
-    # every group launches the dominant kernel once per step: bytes per launch is the mean over groups
-    achieved = dom_bytes / (per_launch_ms * 1e-3) / 1e9 if dom_bytes and per_launch_ms > 0 else None
-    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": None,
-                "peak_source": pk["source"], "launches": dom_launches, "ms_per_launch": per_launch_ms,
+    achieved, peak, unit = None, None, None
+    if bound and dom_ms > 0:
+        rate = cost_step * args.steps / (dom_ms * 1e-3)
+        if bound == "hbm":
+            achieved, peak, unit = rate / 1e9, pk["hbm_gbs"], "GB/s"
+        elif bound == "tensor":
+            achieved, peak, unit = rate / 1e12, pk["bf16_tflops"], "TFLOP/s"
+        else:
+            achieved, peak, unit = rate / 1e12, alu_peak_tflops(), "TFLOP/s"
+    # every streaming kernel's own fraction, for context
+    per_kernel = {}
+    for k, (nl, kms) in kernels.items():
+        kb, kc = kernel_cost(k, w, state)
+        if kb == "hbm" and kms > 0:
+            per_kernel[k] = round(kc * args.steps / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
+    roofline = {"bound": bound or "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": (achieved / peak) if achieved and peak else None, "traffic": None,
+                "peak_source": pk["source"] if bound != "alu" else "derived: 152 SMs x 128 FMA x 2 x 2070 MHz",
+                "launches": dom_launches, "ms_per_launch": per_launch_ms,
+                "hbm_frac_by_kernel": per_kernel,
                 "step_hbm_floor_ms": by / (pk["hbm_gbs"] * 1e9) * 1e3,
                 "step_tensor_floor_ms": fl / (pk["bf16_tflops"] * 1e12) * 1e3,
                 "step_frac_of_floor": max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)) * 1e3

@@ -33,7 +33,7 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
                          int* dead, int* status, cudaStream_t st);
 
 // Cholesky + inverse of batch r x r Gram matrices (one CTA each); see qr.cu.
-cudaError_t chol_inv(int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
+cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
                      int ldz, int* dead, int* status, cudaStream_t st);
 // CholeskyQR2 on the tensor cores (3-term bf16 splits, fp32 accuracy); see qr_tc.cu.
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Si
     extern __shared__ float smem[];
     __shared__ int s_bad;
     __shared__ float s_emax;
+    __shared__ __align__(16) float colw[64];
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
     const int nwarps = nt >> 5;
     const size_t rr = (size_t)r * r;
@@ -138,11 +139,19 @@ __global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Si
                     if (!ok) s_bad |= fin ? kStatusPivot : kStatusNonFinite;
                 }
                 if (lane >= c && lane < jb) Lx(J + lane, J + c) = lv;
+                // column c relative to the step: colw[32 + j] = L(J + c + j, J + c)
+                colw[32 + lane - c] = lv;
+                __syncwarp();
+                float cb[32];
 #pragma unroll
-                for (int j = 1; j < 32; ++j) {
-                    const float lk = __shfl_sync(0xffffffffu, lv, (c + j) & 31);   // L(J + c + j, J + c)
-                    if (lane > c && lane >= c + j) w[j] = fmaf(-lv, lk, w[j]);
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(&colw[32 + j]);
+                    cb[j] = v4.x; cb[j + 1] = v4.y; cb[j + 2] = v4.z; cb[j + 3] = v4.w;
                 }
+#pragma unroll
+                for (int j = 1; j < 32; ++j)
+                    if (lane > c && lane >= c + j) w[j] = fmaf(-lv, cb[j], w[j]);
+                __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 31; ++j) w[j] = w[j + 1];
                 w[31] = 0.f;
@@ -298,7 +307,7 @@ static size_t chol_smem_bytes(int r, bool in_smem)
     return in_smem ? ((size_t)r * (r + 1) + 3 * (size_t)r + scratch) * sizeof(float) : (size_t)3 * r * sizeof(float);
 }
 
-cudaError_t chol_inv(int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
+cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
                      int ldz, int* dead, int* status, cudaStream_t st)
 {
     const size_t smem = chol_smem_bytes(r, true);
@@ -310,10 +319,10 @@ cudaError_t chol_inv(int batch, int r, const float* Sin, int nparts, float* Swor
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        return launch("chol_inv_smem", chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, Sin, nparts, Swork,
+        return launch(name, chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, Sin, nparts, Swork,
                       Wbuf, W, Z3, ldz, dead, status);
     }
-    return launch("chol_inv_global", chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
+    return launch(name, chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
                   Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status);
 }
 
@@ -328,7 +337,8 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
                                      LdB<float, true>{src, sp, ldp}, LdB<float, true>{src, sp, ldp},
                                      EpStore{S, ss, r}, st);
         if (e != cudaSuccess) return e;
-        e = chol_inv(batch, r, S, 1, S, W, W, nullptr, 0, dead, status, st);
+        e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, S, 1, S, W, W, nullptr, 0, dead,
+                     status, st);
         if (e != cudaSuccess) return e;
         // P <- P L^{-T}: B(k, j) = L^{-1}[j][k]
         e = gemm_simt<1>("qr_apply", batch, m, r, r, LdA<float, true>{src, sp, ldp}, LdB<float, false>{W, ss, r},

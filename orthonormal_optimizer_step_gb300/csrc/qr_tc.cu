@@ -114,7 +114,8 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                      nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, S6, 6, 3, 1, kSelA, kSelB};
         e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
         if (e != cudaSuccess) return e;
-        e = chol_inv(batch, r, S6, 6, S, W, nullptr, Z3, rp, dead, status, st);
+        e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, S6, 6, S, W, nullptr, Z3, rp, dead,
+                     status, st);
         if (e != cudaSuccess) return e;
         // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
         TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
