@@ -56,9 +56,10 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.Z3 = carve(off, 3 * b * r * rp * h);
         L.S6 = carve(off, 6 * b * r * r * f);
         L.normp = carve(off, b * (size_t)cdiv(n, 32) * rp * f);
+        L.emax = carve(off, b * sizeof(int));
     } else {
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
-        L.T3 = L.P3 = L.Z3 = L.S6 = L.normp = off;
+        L.T3 = L.P3 = L.Z3 = L.S6 = L.normp = L.emax = off;
     }
     L.total = off;
     return L;

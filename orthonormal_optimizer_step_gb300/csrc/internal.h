@@ -14,6 +14,7 @@ struct DionLayout {
     size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Q16;
     size_t T3, P3, Z3, S6;  // CholeskyQR2 operands of the tensor-core path
     size_t normp;           // per-chunk column sums of squares of R
+    size_t emax;            // per matrix max|S - I| of the second CholeskyQR Gram
     size_t total;
 };
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
@@ -34,7 +35,7 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
 
 // Cholesky + inverse of batch r x r Gram matrices (one CTA each); see qr.cu.
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
-                     int ldz, int* dead, int* status, cudaStream_t st);
+                     int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre = nullptr);
 // CholeskyQR2 on the tensor cores (3-term bf16 splits, fp32 accuracy); see qr_tc.cu.
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const struct DionLayout& L, int* status, cudaStream_t st);

@@ -38,7 +38,8 @@ namespace dion {
 // Z = Z3[0] + Z3[1] + Z3[2] to float32 accuracy) for the tensor-core apply.
 template <bool kSmem>
 __global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
-                                                       float* W, bf16* Z3, int ldz, int* dead_g, int* status)
+                                                       float* W, bf16* Z3, int ldz, int* dead_g, int* status,
+                                                       const int* emax_pre)
 {
     extern __shared__ float smem[];
     __shared__ int s_bad;
@@ -58,6 +59,12 @@ __global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Si
     float* rinv_all = (float*)(deadsm + r);                // reciprocal pivots 1 / L(j, j) (0 if dependent)
 #define Lx0(i) (kSmem ? L[(size_t)(i) * ld + (i)] : Sg[(size_t)(i) * r + (i)])
     float* T = kSmem ? rinv_all + r : Wg;                  // (r - 32) x 32 scratch of the inverse
+    // The near-identity inverse was already written by qr_near_identity_kernel
+    // (emax_pre = max|S - I| of this matrix): nothing left to do.
+    if (emax_pre && __int_as_float(emax_pre[b]) <= 1e-4f) {
+        for (int i = tid; i < r; i += nt) dead[i] = 0;
+        return;
+    }
     for (int i = warp; i < r; i += nwarps) {
         for (int k = lane; k < r; k += 32) {
             const size_t e = (size_t)i * r + k;
@@ -308,7 +315,7 @@ static size_t chol_smem_bytes(int r, bool in_smem)
 }
 
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
-                     int ldz, int* dead, int* status, cudaStream_t st)
+                     int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre)
 {
     const size_t smem = chol_smem_bytes(r, true);
     if (smem <= 215 * 1024) {
@@ -320,10 +327,10 @@ cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int n
             attr = true;
         }
         return launch(name, chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, Sin, nparts, Swork,
-                      Wbuf, W, Z3, ldz, dead, status);
+                      Wbuf, W, Z3, ldz, dead, status, emax_pre);
     }
     return launch(name, chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
-                  Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status);
+                  Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status, emax_pre);
 }
 
 cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,

@@ -69,6 +69,43 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, co
     }
 }
 
+// Second CholeskyQR pass of a well-conditioned panel: the summed Gram is
+// S = I + E.  Writes the first-order inverse L^{-1} = I - F, F = strictly
+// lower(E) + diag(E)/2 (error O(E^2)), as three bf16 terms, and max|E| per
+// matrix; the factorization kernel then skips matrices with max|E| <= 1e-4 and
+// factors the others in full (overwriting these terms).
+__global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, const float* __restrict__ S6,
+                                                               bf16* __restrict__ Z3, int* emax)
+{
+    const int b = blockIdx.y;
+    const size_t rr = (size_t)r * r, zs = (size_t)r * ldz;
+    const float* Sb = S6 + (size_t)b * 6 * rr;
+    bf16* z0 = Z3 + (size_t)3 * b * zs;
+    float em = 0.f;
+    const long long total = (long long)r * ldz;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(e / ldz), k = (int)(e % ldz);
+        float v = 0.f;
+        if (k < r) {
+            const size_t o = (size_t)i * r + k;
+            float sv = Sb[o];
+#pragma unroll
+            for (int q = 1; q < 6; ++q) sv += Sb[q * rr + o];
+            const float ev = sv - (i == k ? 1.f : 0.f);
+            em = fmaxf(em, isfinite(ev) ? fabsf(ev) : 1e30f);
+            v = (k < i) ? -sv : (k == i ? 1.f - 0.5f * ev : 0.f);
+        }
+        bf16 h1, h2, h3;
+        split3(v, h1, h2, h3);
+        z0[e] = h1;
+        z0[zs + e] = h2;
+        z0[2 * zs + e] = h3;
+    }
+    for (int o = 16; o > 0; o >>= 1) em = fmaxf(em, __shfl_xor_sync(0xffffffffu, em, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(&emax[b], __float_as_int(em));   // em >= 0: int order = float order
+}
+
 int pick_bn_qr(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 
 cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
@@ -91,6 +128,7 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
     float* S = (float*)(ws + L.S);
     float* W = (float*)(ws + L.W);
     int* dead = (int*)(ws + L.dead);
+    int* emax = (int*)(ws + L.emax);
     const long long mp = (long long)align_up((size_t)m, 8);
     const int bn = pick_bn_qr(r), bna = pick_bn_qr(rp);
 
@@ -114,8 +152,18 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                      nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, S6, 6, 3, 1, kSelA, kSelB};
         e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
         if (e != cudaSuccess) return e;
+        if (pass == 1) {
+            // near-identity inverse on all SMs; the factorization runs only where it does not apply
+            e = cudaMemsetAsync(emax, 0, sizeof(int) * batch, st);
+            if (e != cudaSuccess) return e;
+            const long long tot = (long long)r * rp;
+            e = launch("qr_near_identity", qr_near_identity_kernel,
+                       dim3((unsigned)std::min<long long>(cdiv(tot, 1024), 1024), batch), dim3(256), 0, st, r, rp,
+                       (const float*)S6, Z3, emax);
+            if (e != cudaSuccess) return e;
+        }
         e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, S6, 6, S, W, nullptr, Z3, rp, dead,
-                     status, st);
+                     status, st, pass == 1 ? emax : nullptr);
         if (e != cudaSuccess) return e;
         // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
         TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
