@@ -329,6 +329,14 @@ cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int n
         return launch(name, chol_inv_kernel<true>, dim3(batch), dim3(512), smem, st, r, Sin, nparts, Swork,
                       Wbuf, W, Z3, ldz, dead, status, emax_pre);
     }
+    static bool gattr = false;
+    if (!gattr) {   // 3 r floats of dynamic shared memory: up to 48 KB at r = 4096, plus the static part
+        cudaError_t e = cudaFuncSetAttribute(chol_inv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             96 * 1024);
+        if (e != cudaSuccess) return e;
+        gattr = true;
+    }
+    if (chol_smem_bytes(r, false) > 96 * 1024) return cudaErrorInvalidValue;
     return launch(name, chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
                   Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status, emax_pre);
 }
