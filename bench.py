@@ -235,7 +235,7 @@ def run_gb300(args, rank, world, local_rank):
     # roofline (kernels of different groups do not share the GPU here)
     saved_streams = list(streams)
     streams[:] = [main for _ in state]
-    prof = od.profile(max_launches=64 * args.steps * len(state) + 64)
+    prof = od.profile(max_launches=2048 * args.steps * len(state) + 64)
     ms_seq = timed(dion_step, args.steps, prof) / args.steps
     torch.cuda.synchronize()
     streams[:] = saved_streams
@@ -299,7 +299,7 @@ def run_gb300(args, rank, world, local_rank):
         mms = timed(muon_step, msteps) / msteps
         saved_streams = list(streams)
         streams[:] = [main for _ in state]
-        mprof = od.profile(max_launches=64 * msteps * len(state) * (w.ns_steps + 2))
+        mprof = od.profile(max_launches=64 * msteps * len(state) * (w.ns_steps + 2) + 64)
         mms_seq = timed(muon_step, msteps, mprof) / msteps
         streams[:] = saved_streams
         mk = mprof.read()

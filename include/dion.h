@@ -193,13 +193,17 @@ const char* dion_status_string(dion_status s);
  * dion_profile_end() stops.  After the caller has synchronized, entries are
  * read one kernel name at a time: dion_profile_count() names, and
  * dion_profile_entry(i, ...) gives the name (static string), the number of
- * launches and their summed device time in milliseconds.  Host-side state is
- * global to the process and not thread-safe.
+ * launches and their summed device time in milliseconds.
+ * dion_profile_dropped() counts the launches since dion_profile_begin that
+ * found all max_launches slots taken and were not timed (the totals then
+ * cover only part of the work).  Host-side state is global to the process and
+ * not thread-safe.
  */
 dion_status dion_profile_begin(int max_launches);
 dion_status dion_profile_end(void);
 int dion_profile_count(void);
 dion_status dion_profile_entry(int i, const char** name, int* launches, double* total_ms);
+int dion_profile_dropped(void);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ DION_F32, DION_BF16 = 0, 1
 # The exported symbols of include/dion.h.
 EXPORTS = ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
            "dion_get_status", "dion_status_string", "dion_profile_begin", "dion_profile_end",
-           "dion_profile_count", "dion_profile_entry")
+           "dion_profile_count", "dion_profile_entry", "dion_profile_dropped")
 
 # Muon's published quintic Newton-Schulz coefficients (a, b, c).
 QUINTIC = (3.4445, -4.7750, 2.0315)
@@ -65,11 +65,12 @@ def lib() -> ctypes.CDLL:
         L.dion_profile_begin.argtypes = [c_int]
         L.dion_profile_end.argtypes = []
         L.dion_profile_count.argtypes = []
+        L.dion_profile_dropped.argtypes = []
         L.dion_profile_entry.argtypes = [c_int, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_int),
                                          ctypes.POINTER(ctypes.c_double)]
         for f in ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
                   "dion_get_status", "dion_profile_begin", "dion_profile_end", "dion_profile_count",
-                  "dion_profile_entry"):
+                  "dion_profile_entry", "dion_profile_dropped"):
             getattr(L, f).restype = c_int
         _lib = L
         return L
@@ -234,8 +235,12 @@ class profile:
         return False
 
     def read(self):
-        """{kernel name: (launches, total ms)}; synchronize before calling."""
+        """{kernel name: (launches, total ms)}; synchronize before calling.
+        Raises if launches went untimed because max_launches was too small."""
         L = lib()
+        dropped = L.dion_profile_dropped()
+        if dropped:
+            raise RuntimeError(f"profile: {dropped} launches beyond max_launches={self.max_launches} were not timed")
         cnt = L.dion_profile_count()
         out = {}
         for i in range(cnt):

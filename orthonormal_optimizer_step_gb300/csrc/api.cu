@@ -57,7 +57,17 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.S6 = carve(off, 6 * b * r * r * f);
         L.normp = carve(off, b * (size_t)cdiv(n, 32) * rp * f);
         L.emax = carve(off, b * sizeof(int));
+        L.nbc = chol_block_size(r);
+        if (L.nbc > 0) {
+            const size_t nb = (size_t)L.nbc;
+            L.ZJ = carve(off, 3 * b * nb * nb * h);
+            L.A3 = carve(off, 3 * b * r * nb * h);
+        } else {
+            L.ZJ = L.A3 = off;
+        }
     } else {
+        L.nbc = 0;
+        L.ZJ = L.A3 = off;
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
         L.T3 = L.P3 = L.Z3 = L.S6 = L.normp = L.emax = off;
     }

@@ -16,6 +16,11 @@ typedef __nv_bfloat16 bf16;
 // Bits of the device status word (see dion_get_status).
 enum : int { kStatusPivot = 1, kStatusNonFinite = 2 };
 
+// A Gram matrix S = I + E with max|E| <= kNearIdentityTol takes the
+// first-order inverse of its Cholesky factor, I - strictly_lower(E) - diag(E)/2
+// (error O(E^2), below float32 rounding).
+constexpr float kNearIdentityTol = 1e-4f;
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v);

@@ -15,6 +15,8 @@ struct DionLayout {
     size_t T3, P3, Z3, S6;  // CholeskyQR2 operands of the tensor-core path
     size_t normp;           // per-chunk column sums of squares of R
     size_t emax;            // per matrix max|S - I| of the second CholeskyQR Gram
+    int nbc;                // block size of the blocked Cholesky (0: one CTA per matrix)
+    size_t ZJ, A3;          // its diagonal-block inverse and panel terms
     size_t total;
 };
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
@@ -33,9 +35,23 @@ MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt);
 cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,
                          int* dead, int* status, cudaStream_t st);
 
+// Where the Gram matrices of chol_inv_io are read: matrix b starts at
+// Sin + b * mstride, its partial q at + q * pstride, row i at + i * lds;
+// dependent-column flags of matrix b at dead + b * dstride.
+struct CholIn {
+    long long mstride, pstride;
+    int lds;
+    long long dstride;
+};
 // Cholesky + inverse of batch r x r Gram matrices (one CTA each); see qr.cu.
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
                      int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre = nullptr);
+cudaError_t chol_inv_io(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
+                        float* W, bf16* Z3, int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre,
+                        CholIn in);
+// Block size of the tensor-core CholeskyQR2's factorization for rank r
+// (0: one CTA per matrix, no blocking).
+int chol_block_size(int r);
 // CholeskyQR2 on the tensor cores (3-term bf16 splits, fp32 accuracy); see qr_tc.cu.
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const struct DionLayout& L, int* status, cudaStream_t st);

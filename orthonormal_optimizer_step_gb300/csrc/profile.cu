@@ -11,7 +11,7 @@ namespace {
 struct Rec { const char* name; cudaEvent_t a, b; };
 struct State {
     bool on = false;
-    int cap = 0, used = 0;
+    int cap = 0, used = 0, dropped = 0;
     std::vector<Rec> recs;
     // aggregated results (filled by dion_profile_count)
     std::vector<const char*> names;
@@ -27,14 +27,18 @@ void release()
         if (r.b) cudaEventDestroy(r.b);
     }
     g.recs.clear();
-    g.cap = g.used = 0;
+    g.cap = g.used = g.dropped = 0;
 }
 
 }  // namespace
 
 int prof_begin(const char* name, cudaStream_t s)
 {
-    if (!g.on || g.used >= g.cap) return -1;
+    if (!g.on) return -1;
+    if (g.used >= g.cap) {
+        ++g.dropped;
+        return -1;
+    }
     const int slot = g.used++;
     g.recs[slot].name = name;
     cudaEventRecord(g.recs[slot].a, s);
@@ -63,6 +67,7 @@ extern "C" dion_status dion_profile_begin(int max_launches)
     }
     g.cap = max_launches;
     g.used = 0;
+    g.dropped = 0;
     g.names.clear(); g.launches.clear(); g.ms.clear();
     g.on = true;
     return DION_OK;
@@ -98,3 +103,5 @@ extern "C" dion_status dion_profile_entry(int i, const char** name, int* launche
     *total_ms = g.ms[i];
     return DION_OK;
 }
+
+extern "C" int dion_profile_dropped(void) { return g.dropped; }

@@ -10,6 +10,8 @@
 // The GEMM walks these as six K segments that pick the split of each operand.
 // The Gram runs the segments as six separate partial products (more CTAs on
 // the small r x r output); the factorization kernel sums them on load.
+#include <algorithm>
+
 #include "internal.h"
 #include "tc_gemm.cuh"
 #include "tmap.h"
@@ -31,10 +33,11 @@ __device__ __forceinline__ void split3(float v, bf16& h1, bf16& h2, bf16& h3)
 }
 
 // P (m x rp fp32, pitch rp) -> P3[3b + t] (m x rp, natural) and T3[3b + t]
-// (rp x mp, transposed), t = 0, 1, 2 the three bf16 terms.
-// P may be given as nparts split partials (summed here, pitch pstride).
-__global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, const float* P, int nparts,
-                                                       long long pstride, bf16* P3, bf16* T3)
+// (rp x mp, transposed), t = 0, 1, 2 the three bf16 terms; columns r..rp-1
+// are written as zero.  P may be given as nparts split partials (summed here,
+// pitch pstride); Pf, if set, receives the float32 sum (pitch rp).
+__global__ void __launch_bounds__(256) qr_split_kernel(int m, int r, int rp, int mp, const float* P, int nparts,
+                                                       long long pstride, bf16* P3, bf16* T3, float* Pf)
 {
     __shared__ float tile[32][33];
     const int b = blockIdx.z, c0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
@@ -44,8 +47,11 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, co
         float v = 0.f;
         if (i < m && c < rp) {
             const size_t o = (size_t)b * pn + (size_t)i * rp + c;
-            v = P[o];
-            for (int q = 1; q < nparts; ++q) v += P[o + q * pstride];
+            if (c < r) {
+                v = P[o];
+                for (int q = 1; q < nparts; ++q) v += P[o + q * pstride];
+            }
+            if (Pf) Pf[o] = v;
             bf16 h1, h2, h3;
             split3(v, h1, h2, h3);
             bf16* po = P3 + (size_t)3 * b * pn + (size_t)i * rp + c;
@@ -72,14 +78,15 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int rp, int mp, co
 // Second CholeskyQR pass of a well-conditioned panel: the summed Gram is
 // S = I + E.  Writes the first-order inverse L^{-1} = I - F, F = strictly
 // lower(E) + diag(E)/2 (error O(E^2)), as three bf16 terms, and max|E| per
-// matrix; the factorization kernel then skips matrices with max|E| <= 1e-4 and
-// factors the others in full (overwriting these terms).
+// matrix; the factorization then runs only for matrices with max|E| above
+// kNearIdentityTol (overwriting these terms).  Only the lower triangle of S is
+// read (S is symmetric; the blocked path computes only that half).
 __global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, const float* __restrict__ S6,
-                                                               bf16* __restrict__ Z3, int* emax)
+                                                               int nparts, bf16* __restrict__ Z3, int* emax)
 {
     const int b = blockIdx.y;
     const size_t rr = (size_t)r * r, zs = (size_t)r * ldz;
-    const float* Sb = S6 + (size_t)b * 6 * rr;
+    const float* Sb = S6 + (size_t)b * nparts * rr;
     bf16* z0 = Z3 + (size_t)3 * b * zs;
     float em = 0.f;
     const long long total = (long long)r * ldz;
@@ -87,14 +94,13 @@ __global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, c
          e += (long long)gridDim.x * blockDim.x) {
         const int i = (int)(e / ldz), k = (int)(e % ldz);
         float v = 0.f;
-        if (k < r) {
+        if (k <= i) {
             const size_t o = (size_t)i * r + k;
             float sv = Sb[o];
-#pragma unroll
-            for (int q = 1; q < 6; ++q) sv += Sb[q * rr + o];
+            for (int q = 1; q < nparts; ++q) sv += Sb[q * rr + o];
             const float ev = sv - (i == k ? 1.f : 0.f);
             em = fmaxf(em, isfinite(ev) ? fabsf(ev) : 1e30f);
-            v = (k < i) ? -sv : (k == i ? 1.f - 0.5f * ev : 0.f);
+            v = (k < i) ? -sv : 1.f - 0.5f * ev;
         }
         bf16 h1, h2, h3;
         split3(v, h1, h2, h3);
@@ -106,6 +112,67 @@ __global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, c
     if ((threadIdx.x & 31) == 0) atomicMax(&emax[b], __float_as_int(em));   // em >= 0: int order = float order
 }
 
+__device__ __forceinline__ bool gated_off(const int* gate, int b)
+{
+    return gate && __int_as_float(gate[b]) <= kNearIdentityTol;
+}
+
+// S[b] = sum of the nparts partial Grams S6[nparts * b + q] (r x r each).
+__global__ void __launch_bounds__(256) qr_sum_kernel(long long rr, int nparts, const float* __restrict__ S6,
+                                                     float* __restrict__ S, const int* gate)
+{
+    const int b = blockIdx.y;
+    if (gated_off(gate, b)) return;
+    const float* src = S6 + (size_t)b * nparts * rr;
+    float* dst = S + (size_t)b * rr;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    if ((rr & 3) == 0) {
+        for (long long e = 4 * ((long long)blockIdx.x * blockDim.x + threadIdx.x); e < rr; e += 4 * stride) {
+            float4 v = *reinterpret_cast<const float4*>(src + e);
+            for (int q = 1; q < nparts; ++q) {
+                const float4 u = *reinterpret_cast<const float4*>(src + q * rr + e);
+                v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+            }
+            *reinterpret_cast<float4*>(dst + e) = v;
+        }
+    } else {
+        for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < rr; e += stride) {
+            float v = src[e];
+            for (int q = 1; q < nparts; ++q) v += src[q * rr + e];
+            dst[e] = v;
+        }
+    }
+}
+
+// Panel of the blocked factorization: rows x w block of S (pitch r, matrix
+// pitch r*r) -> three bf16 terms A3[3b + t] (rows x nb, pitch nb, term pitch
+// r*nb), columns w..nb-1 zero.
+__global__ void __launch_bounds__(256) qr_panel_split_kernel(int r, int rows, int w, int nb, const float* __restrict__ S,
+                                                             bf16* __restrict__ A3, const int* gate)
+{
+    const int b = blockIdx.y;
+    if (gated_off(gate, b)) return;
+    const float* Sb = S + (size_t)b * r * r;
+    const size_t ts = (size_t)r * nb;
+    bf16* a0 = A3 + (size_t)3 * b * ts;
+    const long long total = (long long)rows * nb;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(e / nb), c = (int)(e % nb);
+        const float v = c < w ? Sb[(size_t)i * r + c] : 0.f;
+        bf16 h1, h2, h3;
+        split3(v, h1, h2, h3);
+        a0[e] = h1;
+        a0[ts + e] = h2;
+        a0[2 * ts + e] = h3;
+    }
+}
+
+// Panels up to this rank are factored by one CTA per matrix (the matrix held
+// in shared memory); wider ones by the blocked path with blocks of kCholBlock.
+constexpr int kCholOneCtaMaxR = 248;
+constexpr int kCholBlock = 128;
+
 int pick_bn_qr(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 
 cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
@@ -116,7 +183,128 @@ cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUte
     return tc_gemm<256>(name, ta, tb, K, ep, st);
 }
 
+bool tmap_bf16(CUtensorMap* t, const bf16* base, long long inner, long long rows, long long nz, long long ld,
+               long long zs, int box_rows)
+{
+    return make_tmap_3d(t, base, TmapType::BF16, inner, rows, nz, ld * 2, zs * 2, 64, box_rows);
+}
+
+TcGemmEpi six_term_epi(int M, int N, int bn, int batch, int* status, const int* gate)
+{
+    TcGemmEpi ep{};
+    ep.M = M;
+    ep.N = N;
+    ep.tiles_m = (int)cdiv(M, 128);
+    ep.tiles_n = (int)cdiv(N, bn);
+    ep.batch = batch;
+    ep.alpha = 0.f;
+    ep.beta = 1.f;
+    ep.status = status;
+    ep.nseg = 6;
+    ep.zmul = 3;
+    ep.seg_batch = 0;
+    ep.asel = kSelA;
+    ep.bsel = kSelB;
+    ep.gate = gate;
+    return ep;
+}
+
+// Blocked Cholesky S = L L^T (block size nb; the lower triangle of S is read
+// and overwritten) fused with the triangular solve dst = Psrc L^{-T}, for
+// panels too wide for one CTA.  Per block column J (columns j0 .. j0 + w):
+//   Z_JJ = L_JJ^{-1}                 one CTA per matrix (chol_inv, in shared memory)
+//   L_PJ = S_PJ Z_JJ^T               panel below the diagonal block
+//   S_T -= L_PJ L_PJ^T               trailing lower triangle
+//   Y_J  = P_J - X_{<J} L_{J,<J}^T   forward substitution ...
+//   X_J  = Y_J Z_JJ^T                ... and the diagonal block
+// All products are six-term split GEMMs (float32 accuracy).  L lives only as
+// its three bf16 terms in L3 (r x rp, pitch rp); the terms of X and Y replace
+// those of P in P3 column block by column block.  Matrices whose gate entry is
+// at most kNearIdentityTol are skipped by every kernel.
+cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const float* Psrc, float* dst, bf16* P16,
+                               float* S, float* W, bf16* ZJ, bf16* A3, bf16* L3, bf16* P3, int* dead, int* status,
+                               const int* gate, cudaStream_t st)
+{
+    const int nblk = (int)cdiv(r, nb);
+    const long long z3 = 3ll * batch, rr = (long long)r * r, mrp = (long long)m * rp, rrp = (long long)r * rp;
+    for (int J = 0; J < nblk; ++J) {
+        const int j0 = J * nb, w = std::min(nb, r - j0), rest = r - j0 - w;
+        const int bnw = pick_bn_qr(w);
+        cudaError_t e = chol_inv_io("chol_blk_diag", batch, w, S + (size_t)j0 * r + j0, 1, S, W, nullptr, ZJ, nb,
+                                    dead + j0, status, st, gate, CholIn{rr, 0, r, r});
+        if (e != cudaSuccess) return e;
+        CUtensorMap tZ;
+        if (!tmap_bf16(&tZ, ZJ, nb, w, z3, nb, (long long)w * nb, bnw)) return cudaErrorInvalidValue;
+        if (rest > 0) {
+            const long long tot = (long long)rest * nb;
+            e = launch("chol_blk_split", qr_panel_split_kernel,
+                       dim3((unsigned)std::min<long long>(cdiv(tot, 256), 2048), batch), dim3(256), 0, st, r, rest,
+                       w, nb, (const float*)(S + (size_t)(j0 + w) * r + j0), A3, gate);
+            if (e != cudaSuccess) return e;
+            CUtensorMap tA;
+            if (!tmap_bf16(&tA, A3, nb, rest, z3, nb, (long long)r * nb, 128)) return cudaErrorInvalidValue;
+            TcGemmEpi ep = six_term_epi(rest, w, bnw, batch, status, gate);
+            ep.Cs3 = L3 + (size_t)(j0 + w) * rp + j0;
+            ep.ldcs3 = rp;
+            ep.scs3 = rrp;
+            e = gemm_any(bnw, "chol_blk_panel", tA, tZ, w, ep, st);
+            if (e != cudaSuccess) return e;
+            const int bnt = pick_bn_qr(rest);
+            const bf16* lp = L3 + (size_t)(j0 + w) * rp + j0;
+            CUtensorMap tLa, tLb;
+            if (!tmap_bf16(&tLa, lp, w, rest, z3, rp, rrp, 128) || !tmap_bf16(&tLb, lp, w, rest, z3, rp, rrp, bnt))
+                return cudaErrorInvalidValue;
+            TcGemmEpi et = six_term_epi(rest, rest, bnt, batch, status, gate);
+            et.Cf = S + (size_t)(j0 + w) * r + j0 + w;
+            et.ldc = r;
+            et.sc = rr;
+            et.auxf = et.Cf;
+            et.ldauxf = r;
+            et.sauxf = rr;
+            et.alpha = 1.f;
+            et.beta = -1.f;
+            et.lower = 1;
+            e = gemm_any(bnt, "chol_blk_trail", tLa, tLb, w, et, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (J > 0) {
+            CUtensorMap tX, tL;
+            if (!tmap_bf16(&tX, P3, j0, m, z3, rp, mrp, 128) ||
+                !tmap_bf16(&tL, L3 + (size_t)j0 * rp, j0, w, z3, rp, rrp, bnw))
+                return cudaErrorInvalidValue;
+            TcGemmEpi e1 = six_term_epi(m, w, bnw, batch, status, gate);
+            e1.auxf = Psrc + j0;
+            e1.ldauxf = rp;
+            e1.sauxf = mrp;
+            e1.alpha = 1.f;
+            e1.beta = -1.f;
+            e1.Cs3 = P3 + j0;
+            e1.ldcs3 = rp;
+            e1.scs3 = mrp;
+            e = gemm_any(bnw, "chol_blk_solve", tX, tL, j0, e1, st);
+            if (e != cudaSuccess) return e;
+        }
+        CUtensorMap tY;
+        if (!tmap_bf16(&tY, P3 + j0, w, m, z3, rp, mrp, 128)) return cudaErrorInvalidValue;
+        TcGemmEpi e2 = six_term_epi(m, w, bnw, batch, status, gate);
+        e2.Cf = dst + j0;
+        e2.C = P16 ? P16 + j0 : nullptr;
+        e2.ldc = rp;
+        e2.sc = mrp;
+        if (J + 1 < nblk) {
+            e2.Cs3 = P3 + j0;
+            e2.ldcs3 = rp;
+            e2.scs3 = mrp;
+        }
+        e = gemm_any(bnw, "chol_blk_apply", tY, tZ, w, e2, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
+
+int chol_block_size(int r) { return r > kCholOneCtaMaxR ? kCholBlock : 0; }
 
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st)
@@ -131,6 +319,10 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
     int* emax = (int*)(ws + L.emax);
     const long long mp = (long long)align_up((size_t)m, 8);
     const int bn = pick_bn_qr(r), bna = pick_bn_qr(rp);
+    const bool blocked = L.nbc > 0;
+    // blocked: the Gram's lower half, accumulated straight into S when that
+    // alone fills the SMs, else as six partials summed afterwards
+    const bool direct = blocked && cdiv(r, 128) * cdiv(r, bn) * batch / 2 >= num_sms();
 
     CUtensorMap tTa, tTb, tPa, tZb;
     if (!make_tmap_3d(&tTa, T3, TmapType::BF16, m, rp, 3ll * batch, mp * 2, (long long)rp * mp * 2, 64, 128) ||
@@ -145,12 +337,23 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
         float* dst = pass == 0 ? Ptmp : P;
         const int np_ = pass == 0 ? nparts : 1;
         cudaError_t e = launch("qr_split", qr_split_kernel, dim3((unsigned)cdiv(rp, 32), (unsigned)cdiv(m, 32), batch),
-                               dim3(32, 8), 0, st, m, rp, (int)mp, src, np_, (long long)batch * m * rp, P3, T3);
+                               dim3(32, 8), 0, st, m, r, rp, (int)mp, src, np_, (long long)batch * m * rp, P3, T3,
+                               (blocked && pass == 0) ? dst : (float*)nullptr);
         if (e != cudaSuccess) return e;
-        // six partial Grams S6[6b + q] = T_a(q) T_b(q)^T  (r x r)
-        TcGemmEpi eg{r, r, (int)cdiv(r, 128), (int)cdiv(r, bn), 6 * batch, nullptr, r, (long long)r * r,
-                     nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, S6, 6, 3, 1, kSelA, kSelB};
-        e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
+        if (direct) {
+            TcGemmEpi eg = six_term_epi(r, r, bn, batch, status, nullptr);
+            eg.Cf = S;
+            eg.ldc = r;
+            eg.sc = (long long)r * r;
+            eg.lower = 1;
+            e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
+        } else {
+            // six partial Grams S6[6b + q] = T_a(q) T_b(q)^T  (r x r)
+            TcGemmEpi eg{r, r, (int)cdiv(r, 128), (int)cdiv(r, bn), 6 * batch, nullptr, r, (long long)r * r,
+                         nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, S6, 6, 3, 1, kSelA, kSelB};
+            eg.lower = blocked ? 1 : 0;
+            e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
+        }
         if (e != cudaSuccess) return e;
         if (pass == 1) {
             // near-identity inverse on all SMs; the factorization runs only where it does not apply
@@ -159,17 +362,42 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
             const long long tot = (long long)r * rp;
             e = launch("qr_near_identity", qr_near_identity_kernel,
                        dim3((unsigned)std::min<long long>(cdiv(tot, 1024), 1024), batch), dim3(256), 0, st, r, rp,
-                       (const float*)S6, Z3, emax);
+                       (const float*)(direct ? S : S6), direct ? 1 : 6, Z3, emax);
             if (e != cudaSuccess) return e;
         }
-        e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, S6, 6, S, W, nullptr, Z3, rp, dead,
-                     status, st, pass == 1 ? emax : nullptr);
-        if (e != cudaSuccess) return e;
-        // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
-        TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
-                     (long long)m * rp, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, dst, 6, 3, 0, kSelA, kSelB};
-        e = gemm_any(bna, "qr_apply_tc", tPa, tZb, rp, ea, st);
-        if (e != cudaSuccess) return e;
+        const int* gate = pass == 1 ? emax : nullptr;
+        if (!blocked) {
+            // first pass: the six partials summed on all SMs, so the one-CTA
+            // factorization reads one matrix; the second pass factors only
+            // matrices that failed the near-identity test and reads the partials
+            if (pass == 0) {
+                const long long rr = (long long)r * r;
+                e = launch("qr_gram_sum", qr_sum_kernel, dim3((unsigned)std::min<long long>(cdiv(rr, 1024), 1024), batch),
+                           dim3(256), 0, st, rr, 6, (const float*)S6, S, (const int*)nullptr);
+                if (e != cudaSuccess) return e;
+            }
+            e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, pass == 0 ? S : S6, pass == 0 ? 1 : 6,
+                         S, W, nullptr, Z3, rp, dead, status, st, gate);
+            if (e != cudaSuccess) return e;
+        }
+        if (!blocked || pass == 1) {
+            // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
+            TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
+                         (long long)m * rp, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, dst, 6, 3, 0, kSelA, kSelB};
+            e = gemm_any(bna, "qr_apply_tc", tPa, tZb, rp, ea, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (blocked) {
+            if (!direct) {
+                const long long rr = (long long)r * r;
+                e = launch("qr_gram_sum", qr_sum_kernel, dim3((unsigned)std::min<long long>(cdiv(rr, 1024), 1024), batch),
+                           dim3(256), 0, st, rr, 6, (const float*)S6, S, gate);
+                if (e != cudaSuccess) return e;
+            }
+            e = chol_blocked_apply(batch, m, r, rp, L.nbc, pass == 0 ? dst : src, dst, pass == 1 ? P16 : nullptr, S, W,
+                                   (bf16*)(ws + L.ZJ), (bf16*)(ws + L.A3), Z3, P3, dead, status, gate, st);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -35,6 +35,16 @@ struct TcGemmEpi {
     // output matrix (index nseg*b + q) instead of being accumulated.
     int nseg, zmul, seg_batch;
     uint32_t asel, bsel;
+    // float32 addend (used instead of aux when set): C = alpha * auxf + beta * acc
+    const float* auxf; long long ldauxf, sauxf;
+    // three-term bf16 split of the result (X = X1 + X2 + X3), term t of matrix b
+    // at Cs3 + (3b + t) * scs3 + row * ldcs3 + col
+    bf16* Cs3; long long ldcs3, scs3;
+    // tiles that run: with `gate`, only those of matrices b whose gate[b]
+    // (a float max|S - I| stored as int bits) exceeds kNearIdentityTol; with
+    // `lower`, only tiles holding an element on or below the diagonal
+    const int* gate;
+    int lower;
 };
 
 template <int BN>
@@ -54,13 +64,37 @@ int num_sms();
 // that includes it owns its own copy (and its own one-time attribute setup).
 namespace {
 
+__device__ __forceinline__ bool tc_tile_on(const TcGemmEpi& ep, int b, int tm, int tn, int bm_rows, int bn_cols)
+{
+    if (ep.lower && tn * bn_cols > tm * bm_rows + bm_rows - 1) return false;
+    if (ep.gate) {
+        const int bm = ep.seg_batch ? b / ep.nseg : b;
+        if (__int_as_float(ep.gate[bm]) <= kNearIdentityTol) return false;
+    }
+    return true;
+}
+
 __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row, int col0, const uint32_t (&v)[32])
 {
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = ep.beta * __uint_as_float(v[i]);
     const int ncol = min(32, ep.N - col0);
-    if (ep.aux) {
+    if (ep.auxf) {
+        const float* ap = ep.auxf + b * ep.sauxf + (long long)row * ep.ldauxf + col0;
+        if (ncol == 32 && ((uintptr_t)ap & 15u) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 u = *reinterpret_cast<const float4*>(ap + j);
+                acc[j] = fmaf(ep.alpha, u.x, acc[j]);
+                acc[j + 1] = fmaf(ep.alpha, u.y, acc[j + 1]);
+                acc[j + 2] = fmaf(ep.alpha, u.z, acc[j + 2]);
+                acc[j + 3] = fmaf(ep.alpha, u.w, acc[j + 3]);
+            }
+        } else {
+            for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, ap[i], acc[i]);
+        }
+    } else if (ep.aux) {
         const bf16* ap = ep.aux + b * ep.saux + (long long)row * ep.ldaux + col0;
         if (ncol == 32) {
 #pragma unroll
@@ -74,9 +108,48 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
             for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, __bfloat162float(ap[i]), acc[i]);
         }
     }
+    if (ep.Cs3) {
+        bf16* sp = ep.Cs3 + (long long)3 * b * ep.scs3 + (long long)row * ep.ldcs3 + col0;
+        if (ncol == 32 && ((uintptr_t)sp & 15u) == 0 && (ep.scs3 & 7) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint32_t t1[4], t2[4], t3[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    uint32_t w1 = 0, w2 = 0, w3 = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float v = acc[j + e + h];
+                        const bf16 h1 = __float2bfloat16_rn(v);
+                        const float r1 = v - __bfloat162float(h1);
+                        const bf16 h2 = __float2bfloat16_rn(r1);
+                        const bf16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+                        w1 |= (uint32_t)__bfloat16_as_ushort(h1) << (16 * h);
+                        w2 |= (uint32_t)__bfloat16_as_ushort(h2) << (16 * h);
+                        w3 |= (uint32_t)__bfloat16_as_ushort(h3) << (16 * h);
+                    }
+                    t1[e / 2] = w1;
+                    t2[e / 2] = w2;
+                    t3[e / 2] = w3;
+                }
+                *reinterpret_cast<uint4*>(sp + j) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+                *reinterpret_cast<uint4*>(sp + ep.scs3 + j) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+                *reinterpret_cast<uint4*>(sp + 2 * ep.scs3 + j) = make_uint4(t3[0], t3[1], t3[2], t3[3]);
+            }
+        } else {
+            for (int i = 0; i < ncol; ++i) {
+                const bf16 h1 = __float2bfloat16_rn(acc[i]);
+                const float r1 = acc[i] - __bfloat162float(h1);
+                const bf16 h2 = __float2bfloat16_rn(r1);
+                sp[i] = h1;
+                sp[ep.scs3 + i] = h2;
+                sp[2 * ep.scs3 + i] = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+            }
+        }
+    }
     if (ep.Cf) {
         float* fp = ep.Cf + b * ep.sc + (long long)row * ep.ldc + col0;
-        if (ncol == 32 && (ep.ldc & 3) == 0) {
+        if (ncol == 32 && ((uintptr_t)fp & 15u) == 0) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(fp + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
@@ -85,6 +158,7 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
         }
         if (!ep.C) return;             // else also a bf16 copy with the same pitches
     }
+    if (!ep.C) return;
     bf16* cp = ep.C + b * ep.sc + (long long)row * ep.ldc + col0;
     if (ncol == 32) {
 #pragma unroll
@@ -154,6 +228,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
                 const int b = t / per_mat, rem = t % per_mat;
                 const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+                if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
                 const int q0 = ep.seg_batch ? b % ep.nseg : 0, q1 = ep.seg_batch ? q0 + 1 : ep.nseg;
                 const int bm = ep.seg_batch ? b / ep.nseg : b;
                 for (int q = q0; q < q1; ++q) {
@@ -176,7 +251,11 @@ __global__ void __launch_bounds__(192, 1)
             int stage = 0;
             uint32_t ph = 0;
             int it = 0;
-            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
+                {
+                    const int b = t / per_mat, rem = t % per_mat;
+                    if (!tc_tile_on(ep, b, rem / ep.tiles_n, rem % ep.tiles_n, Cfg::BM, BN)) continue;
+                }
                 const int buf = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!tc::mbar_wait(&acc_empty[buf], aph ^ 1, abrt, ep.status)) break;
@@ -198,18 +277,21 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (!ok) break;
                 tc::mma_commit(&acc_full[buf]);
+                ++it;
             }
         }
     } else {
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         int it = 0;
-        for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
-            const int buf = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
-            if (!tc::mbar_wait(&acc_full[buf], aph, abrt, ep.status)) break;
-            tc::tc_fence_after();
+        for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
             const int b = t / per_mat, rem = t % per_mat;
             const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+            if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
+            const int buf = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            ++it;
+            if (!tc::mbar_wait(&acc_full[buf], aph, abrt, ep.status)) break;
+            tc::tc_fence_after();
             const int row = tm * Cfg::BM + q * 32 + lane;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {

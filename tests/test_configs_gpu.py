@@ -43,6 +43,10 @@ def _check_dion_group(g, r, dtype, mu, lr, wd, g_std, seed, bi=0):
     X, M, Q = wl.make_state(g, r, dtype, DEV, seed)
     M = wl.make_momentum(g, g_std, DEV, seed)
     G = wl.make_grad(g, g_std, dtype, DEV, seed, step=1)
+    return _check_dion_tensors(g, r, dtype, X, G, M, Q, mu, lr, wd, seed, bi)
+
+
+def _check_dion_tensors(g, r, dtype, X, G, M, Q, mu, lr, wd, seed, bi):
     X0, M0, Q0 = X[bi].double(), M[bi].double(), Q[bi].double()
     B = M0 + G[bi].double()
     ws = od.dion_step_batched(X, G, M, Q, mu=mu, lr=lr, weight_decay=wd)
@@ -107,6 +111,28 @@ def test_square_sweep_dion(n, frac):
     g = w.groups[0]
     out = _check_dion_group(g, g.rank(frac), w.dtype, w.mu, w.lr, w.wd, w.g_std, seed=6000 + n, bi=3)
     _assert_dion(out, w.dtype)
+
+
+@pytest.mark.parametrize("r", [96, 320])
+def test_ill_conditioned_panel_takes_full_second_pass(r):
+    """B = G with singular values 1 .. 1e-6 (geometric) and M = 0: B Q has a
+    condition number in the hundreds, so after the first CholeskyQR pass
+    P^T P - I is far above the near-identity threshold and the second pass
+    factors in full (one CTA per matrix at rank 96, blocked at rank 320).
+    P must still come out orthonormal, spanning B Q."""
+    g = wl.Group(2, 1024, 768)
+    gen = torch.Generator(device="cpu").manual_seed(91)
+    Gs = []
+    for _ in range(g.batch):
+        U, _ = torch.linalg.qr(torch.randn(g.m, g.n, generator=gen, dtype=torch.float64))
+        V, _ = torch.linalg.qr(torch.randn(g.n, g.n, generator=gen, dtype=torch.float64))
+        s = torch.logspace(0, -6, g.n, dtype=torch.float64)
+        Gs.append((U * s) @ V.T * 30.0)
+    G = torch.stack(Gs).to(torch.bfloat16).to(DEV)
+    X, _, Q = wl.make_state(g, r, torch.bfloat16, DEV, 91)
+    M = torch.zeros(g.batch, g.m, g.n, dtype=torch.float32, device=DEV)
+    out = _check_dion_tensors(g, r, torch.bfloat16, X, G, M, Q, 0.9, 0.01, 0.0, 91, 1)
+    _assert_dion(out, torch.bfloat16)
 
 
 def _check_ns_group(g, dtype, seed, bi=0, steps=5):

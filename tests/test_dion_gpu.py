@@ -47,6 +47,8 @@ RAGGED = [
     (2, 130, 260, 17, torch.bfloat16),
     (1, 64, 64, 16, torch.bfloat16),
     (1, 1024, 1024, 288, torch.bfloat16),  # r > 256: two 256-column chunks of the rank
+    (2, 700, 600, 300, torch.bfloat16),    # blocked factorization: blocks of 128, 128, 44
+    (1, 1100, 1300, 520, torch.bfloat16),  # blocked factorization: four blocks and a ragged 8
     (1, 8, 520, 3, torch.bfloat16),        # very wide
     (2, 520, 8, 8, torch.float32),         # very tall, full rank
 ]
@@ -154,3 +156,26 @@ def test_streams_and_reused_workspace():
         od.dion_step_batched(X, G, M, Q, mu=0.9, lr=0.1, weight_decay=0.0, workspace=ws, stream=s)
     s.synchronize()
     assert torch.equal(X, A[0]) and torch.equal(M, A[1]) and torch.equal(Q, A[2])
+
+
+def test_blocked_factorization_reads_no_stale_workspace():
+    """Rank 300 takes the blocked factorization, which computes only the lower
+    half of each Gram matrix: a workspace full of NaN bit patterns gives the
+    same bits as a zeroed one."""
+    g = wl.Group(2, 640, 512)
+    r = 300
+    X, M, Q = wl.make_state(g, r, torch.bfloat16, DEV, seed=31)
+    G = wl.make_grad(g, 1.0, torch.bfloat16, DEV, 31, 0)
+    n_ws = od.dion_workspace_size(2, 640, 512, r, od.DION_BF16)
+    outs = []
+    for fill in (0x00, 0xFF):
+        A = [t.clone() for t in (X, M, Q)]
+        ws = od.new_workspace(n_ws, DEV)
+        ws.fill_(fill)
+        od.dion_step_batched(A[0], G, A[1], A[2], mu=0.9, lr=0.1, weight_decay=0.0, workspace=ws)
+        torch.cuda.synchronize()
+        assert od.dion_get_status(ws) == 0
+        outs.append(A)
+    for a, b in zip(*outs):
+        assert torch.isfinite(a.float()).all()
+        assert torch.equal(a, b)
