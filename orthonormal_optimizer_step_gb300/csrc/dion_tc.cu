@@ -108,7 +108,9 @@ struct PassArgs {
     int* status;
 };
 
-constexpr int kProducers = 256;   // 8 producer warps; warp 8 issues the MMAs
+constexpr int kProducers = 512;   // 16 producer warps; warp 16 issues the MMAs
+constexpr int kPassWarps = kProducers / 32 + 1;
+constexpr int kPerProducer = 1024 / kProducers;   // 8-element groups of a 128 x 64 tile per producer thread
 constexpr int kStages = 4;
 constexpr uint32_t kAB = kBM * kBK * 2;          // 16 KB bf16 A tile
 constexpr uint32_t kBB = 256 * kBK * 2;          // up to 32 KB B tile
@@ -119,7 +121,7 @@ constexpr size_t kPassSmem = (size_t)kStages * kStage + 1024 + 256;
 // A tile = 128 rows of B x 64 columns, K-major.  MN_A = true: pass 6
 // (R = B^T P), A tile = 64 rows of B x 128 columns, MN-major.
 template <bool MN_A, bool VEC>
-__global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB, PassArgs a)
+__global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB, PassArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -143,14 +145,14 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&full[s], kProducers + 1);
+            tc::mbar_init(&full[s], kProducers / 32 + 1);   // one arrive per producer warp + the TMA
             tc::mbar_init(&empty[s], 1);
         }
         tc::mbar_init(done, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == kPassWarps - 1) {
         tc::tmem_alloc(tmem_slot, 256);
         tc::tmem_relinquish();
     }
@@ -159,16 +161,16 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 8) {
+    if (warp < kPassWarps - 1) {
         // ---------------- producers: B = M + G -> bf16 -> swizzled A tile.
-        // The global loads of chunk kc + 1 are issued before chunk kc is
-        // converted and stored, so two chunks of loads are in flight.
-        Raw8 cur[4], nxt[4];
-        uint32_t off[4];
-        auto fetch = [&](int kc, Raw8 (&dst)[4]) {
+        // The global loads of chunks kc + 1 and kc + 2 are issued before chunk
+        // kc is converted and stored, so three chunks of loads are in flight.
+        Raw8 cur[kPerProducer], nxt[kPerProducer], nxt2[kPerProducer];
+        uint32_t off[kPerProducer];
+        auto fetch = [&](int kc, Raw8 (&dst)[kPerProducer]) {
             const int k0 = (kc0 + kc) * kBK;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kPerProducer; ++u) {
                 const int g = threadIdx.x + kProducers * u;
                 if (!MN_A) {
                     const int row = g >> 3, ch = g & 7;             // 128 rows x 8 chunks
@@ -185,8 +187,9 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
             }
         };
         if (nk > 0) fetch(0, cur);
+        if (nk > 1) fetch(1, nxt);
         for (int kc = 0; kc < nk && !*abrt; ++kc) {
-            if (kc + 1 < nk) fetch(kc + 1, nxt);
+            if (kc + 2 < nk) fetch(kc + 2, nxt2);
             const int stage = kc % kStages;
             const uint32_t ph = (kc / kStages) & 1;
             if (lane == 0) tc::mbar_wait(&empty[stage], ph ^ 1, abrt, a.status);
@@ -204,11 +207,15 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(sA + off[u]) = sum_pack8(cur[u]);
+            for (int u = 0; u < kPerProducer; ++u) *reinterpret_cast<uint4*>(sA + off[u]) = sum_pack8(cur[u]);
             tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&full[stage]);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&full[stage]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+            for (int u = 0; u < kPerProducer; ++u) {
+                cur[u] = nxt[u];
+                nxt[u] = nxt2[u];
+            }
         }
     } else if (lane == 0) {
         // ---------------- MMA issuer
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(288, 1) dion_pass_kernel(const __grid_constant
         tc::tc_fence_before();
     }
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kPassWarps - 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 256);
     }
@@ -715,7 +722,7 @@ static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm
         if (e != cudaSuccess) return e;
         attr[vec] = true;
     }
-    return launch(name, k, grid, dim3(288), kPassSmem, st, tm, pa);
+    return launch(name, k, grid, dim3(kPassWarps * 32), kPassSmem, st, tm, pa);
 }
 
 dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* Gv, float* M, float* Q, float mu,

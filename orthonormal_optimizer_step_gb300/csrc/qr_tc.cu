@@ -173,13 +173,14 @@ __global__ void __launch_bounds__(256) qr_panel_split_kernel(int r, int rows, in
 constexpr int kCholOneCtaMaxR = 248;
 constexpr int kCholBlock = 128;
 
-int pick_bn_qr(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+int pick_bn_qr(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 192 ? 192 : 256)); }
 
 cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
                      cudaStream_t st)
 {
     if (bn == 64) return tc_gemm<64>(name, ta, tb, K, ep, st);
     if (bn == 128) return tc_gemm<128>(name, ta, tb, K, ep, st);
+    if (bn == 192) return tc_gemm<192>(name, ta, tb, K, ep, st);
     return tc_gemm<256>(name, ta, tb, K, ep, st);
 }
 

@@ -4,7 +4,7 @@
 //   C[b] (M x N) = alpha * aux[b] + beta * (A[b] (M x K) . B[b] (N x K)^T)
 //
 // Both operands are K-major (row-major with K contiguous).  One CTA per SM
-// walks the output tiles (BM = 128 rows, BN = 64/128/256 columns) of every
+// walks the output tiles (BM = 128 rows, BN = 64/128/192/256 columns) of every
 // matrix of the batch.  Warp 0 issues TMA loads into a ring of shared-memory
 // stages, warp 1 issues tcgen05.mma from one thread into a double-buffered
 // TMEM accumulator, warps 2..5 drain the accumulator (tcgen05.ld), apply the
@@ -50,11 +50,11 @@ struct TcGemmEpi {
 template <int BN>
 struct TcGemmCfg {
     static constexpr int BM = 128, BK = 64;
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : (BN == 128 ? 6 : 8));
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = BN == 192 ? 512 : 2 * BN;   // a power of two >= 2 BN
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
 };
 
