@@ -136,12 +136,34 @@ def kernel_cost(name, w, state):
             tot += mn * (4 + eb) + g.batch * (g.m * rp * 2 + g.n * rp * 4)
         elif name.startswith("dion_update"):
             tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * rp * 2 + 2 * g.n * rp * 2)
-        elif name.startswith("chol_inv_pass1"):
+        elif name == "chol_inv_pass1":
             bound = "alu"
-            tot += g.batch * (2.0 / 3.0) * r ** 3          # Cholesky r^3/3 + triangular inverse r^3/3
-        elif name.startswith("qr_gram") or name.startswith("qr_apply"):
+            if r <= 248:
+                tot += g.batch * (2.0 / 3.0) * r ** 3      # Cholesky r^3/3 + triangular inverse r^3/3
+        elif name == "qr_gram_tc" or name == "qr_apply_tc":
             bound = "tensor"
             tot += g.batch * 6 * 2.0 * g.m * r * r          # six bf16 cross-term products
+        elif name == "qr_gram_sum":
+            tot += g.batch * (6 * 4 + 4) * r * r            # six fp32 partials in, one out
+        elif name.startswith("chol_blk_"):
+            # blocked factorization (r > 248, blocks of 128), first CholeskyQR pass;
+            # the second pass is gated off for near-identity Grams
+            bound = "alu" if name == "chol_blk_diag" else "tensor"
+            for j0 in range(0, r if r > 248 else 0, 128):
+                wb = min(128, r - j0)
+                rest = r - j0 - wb
+                if name == "chol_blk_diag":
+                    tot += g.batch * (2.0 / 3.0) * wb ** 3
+                elif name == "chol_blk_panel":
+                    tot += g.batch * 6 * 2.0 * rest * wb * wb
+                elif name == "chol_blk_trail":
+                    tot += g.batch * 6 * 2.0 * rest * (rest + 1) / 2 * wb
+                elif name == "chol_blk_solve":
+                    tot += g.batch * 6 * 2.0 * g.m * wb * j0
+                elif name == "chol_blk_apply":
+                    tot += g.batch * 6 * 2.0 * g.m * wb * wb
+                else:
+                    return None, 0.0
         else:
             return None, 0.0
     return bound, tot
