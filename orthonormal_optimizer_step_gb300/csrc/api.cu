@@ -37,26 +37,38 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
     L.P0 = carve(off, b * m * rp * f);
     L.P1 = carve(off, b * m * rp * f);
     L.R = carve(off, b * n * rp * f);
-    L.S = carve(off, b * r * r * f);
+    const size_t nb8 = (size_t)(r + 7) / 8;
+    L.S = carve(off, b * std::max((size_t)r * r, nb8 * (nb8 + 1) / 2 * 64) * f);   // also the block-major Gram
     L.W = carve(off, b * r * r * f);
     L.dead = carve(off, b * r * sizeof(int));
     L.inv = carve(off, b * rp * f);
     if (L.tc) {
         const int rch = (int)cdiv(L.rp, 256);
-        L.ksplit = stream_splits(cdiv(m, 128) * rch * batch, (int)cdiv(n, 64));
-        L.ksplit_r = stream_splits(cdiv(n, 128) * rch * batch, (int)cdiv(m, 64));
+        // wider than one 256-column chunk: B = M + G is formed once in bf16
+        // (row-major and transposed) and both products run as TMA GEMMs
+        L.wide = rch > 1;
+        L.ksplit = L.wide ? 1 : stream_splits(cdiv(m, 128) * rch * batch, (int)cdiv(n, 64));
+        L.ksplit_r = L.wide ? 1 : stream_splits(cdiv(n, 128) * rch * batch, (int)cdiv(m, 64));
         const size_t rows = std::max((size_t)L.ksplit * m, (size_t)L.ksplit_r * n);
         L.Ppart = carve(off, rows * b * rp * f);
         L.Qt16 = carve(off, b * rp * align_up((size_t)n, 8) * h);
         L.P16 = carve(off, b * m * rp * h);
         L.R16 = carve(off, b * n * rp * h);
         L.Q16 = carve(off, b * n * rp * h);
-        L.T3 = carve(off, 3 * b * rp * align_up((size_t)m, 8) * h);
         L.P3 = carve(off, 3 * b * m * rp * h);
+        L.P3b = carve(off, 3 * b * m * rp * h);
         L.Z3 = carve(off, 3 * b * r * rp * h);
         L.S6 = carve(off, 6 * b * r * r * f);
         L.normp = carve(off, b * (size_t)cdiv(n, 32) * rp * f);
         L.emax = carve(off, b * sizeof(int));
+        if (L.wide) {
+            const size_t mp = align_up((size_t)m, 8), np = align_up((size_t)n, 8);
+            L.B16 = carve(off, b * m * np * h);
+            L.B16T = carve(off, b * n * mp * h);
+            L.P16T = carve(off, b * rp * mp * h);
+        } else {
+            L.B16 = L.B16T = L.P16T = off;
+        }
         L.nbc = chol_block_size(r);
         if (L.nbc > 0) {
             const size_t nb = (size_t)L.nbc;
@@ -67,9 +79,10 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         }
     } else {
         L.nbc = 0;
-        L.ZJ = L.A3 = off;
+        L.wide = false;
+        L.ZJ = L.A3 = L.B16 = L.B16T = L.P16T = off;
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
-        L.T3 = L.P3 = L.Z3 = L.S6 = L.normp = L.emax = off;
+        L.P3 = L.P3b = L.Z3 = L.S6 = L.normp = L.emax = off;
     }
     L.total = off;
     return L;

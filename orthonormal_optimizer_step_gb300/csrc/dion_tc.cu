@@ -21,6 +21,7 @@
 // shared memory by TMA (Q, P, R operands) or from the producer warps (B).
 #include "internal.h"
 #include "tc.cuh"
+#include "tc_gemm.cuh"
 #include "tmap.h"
 
 namespace dion {
@@ -417,8 +418,13 @@ struct UpdPArgs {
 constexpr uint32_t kPStage = kUStage;                              // 32 KB of operands per K chunk
 constexpr uint32_t kEM = 2 * 16384, kEG = 16384, kEX = 16384;      // M (two 32-column boxes), G, X
 constexpr uint32_t kEBuf = kEM + kEG + kEX;                        // 64 KB
-constexpr size_t kUpdPSmem = 2 * (size_t)kPStage + 2 * (size_t)kEBuf + 1024 + 256;
+// Ring depths of the persistent update: operand stages per K chunk and M/G/X
+// tile buffers.  Short K ranges (rp <= 256) double-buffer the M/G/X tiles;
+// long ones (wide ranks) trade that for a deeper operand ring.
+template <int OPS, int EPI>
+constexpr size_t upd_smem() { return OPS * (size_t)kPStage + EPI * (size_t)kEBuf + 1024 + 256; }
 
+template <int OPS, int EPI>
 __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
     const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmR,
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmM,
@@ -426,13 +432,13 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* ops = smem;                              // [2][kPStage]
-    uint8_t* epi = smem + 2 * kPStage;                // [2][kEBuf]
-    uint64_t* ofull = (uint64_t*)(epi + 2 * kEBuf);
-    uint64_t* oempty = ofull + 2;
-    uint64_t* efull = oempty + 2;
-    uint64_t* eempty = efull + 2;
-    uint64_t* afull = eempty + 2;
+    uint8_t* ops = smem;                              // [OPS][kPStage]
+    uint8_t* epi = smem + OPS * kPStage;              // [EPI][kEBuf]
+    uint64_t* ofull = (uint64_t*)(epi + EPI * kEBuf);
+    uint64_t* oempty = ofull + OPS;
+    uint64_t* efull = oempty + OPS;
+    uint64_t* eempty = efull + EPI;
+    uint64_t* afull = eempty + EPI;
     uint64_t* aempty = afull + 2;
     uint32_t* tmem_slot = (uint32_t*)(aempty + 2);
     int* abort_flag = (int*)(tmem_slot + 1);
@@ -441,11 +447,15 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
     const int per_mat = a.tiles_m * a.tiles_n, tiles = a.batch * per_mat;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < OPS; ++s) {
             tc::mbar_init(&ofull[s], 1);
             tc::mbar_init(&oempty[s], 1);
+        }
+        for (int s = 0; s < EPI; ++s) {
             tc::mbar_init(&efull[s], 1);
             tc::mbar_init(&eempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&afull[s], 1);
             tc::mbar_init(&aempty[s], 4);
         }
@@ -469,8 +479,8 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
                 const int b = t / per_mat, rem = t % per_mat;
                 const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
-                const int eb = it & 1;
-                if (!tc::mbar_wait(&eempty[eb], ((it >> 1) & 1) ^ 1, abrt, a.status)) break;
+                const int eb = it % EPI;
+                if (!tc::mbar_wait(&eempty[eb], ((it / EPI) & 1) ^ 1, abrt, a.status)) break;
                 uint8_t* e = epi + eb * kEBuf;
                 tc::mbar_arrive_expect_tx(&efull[eb], kEBuf);
                 tc::tma_load_3d(e, &tmM, &efull[eb], n0, m0, b);
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                     tc::tma_load_3d(o, &tmP, &ofull[stage], kc * kBK, m0, b);
                     tc::tma_load_3d(o + kUA, &tmR, &ofull[stage], kc * kBK, n0, b);
                     tc::tma_load_3d(o + kUA + kUB, &tmQ, &ofull[stage], kc * kBK, n0, b);
-                    if (++stage == 2) { stage = 0; ph ^= 1; }
+                    if (++stage == OPS) { stage = 0; ph ^= 1; }
                 }
             }
         }
@@ -511,7 +521,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                         tc::mma_bf16(d + kUBN, ad, tc::make_sdesc(q0 + k * 32, 16, 1024), idesc, (kc | k) != 0);
                     }
                     tc::mma_commit(&oempty[stage]);
-                    if (++stage == 2) { stage = 0; ph ^= 1; }
+                    if (++stage == OPS) { stage = 0; ph ^= 1; }
                 }
                 if (!ok) break;
                 tc::mma_commit(&afull[ab]);
@@ -523,10 +533,10 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
             const int b = t / per_mat, rem = t % per_mat;
             const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
-            const int ab = it & 1, eb = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const int ab = it & 1, eb = it % EPI;
+            const uint32_t aph = (it >> 1) & 1, eph = (it / EPI) & 1;
             const bool ok = tc::mbar_wait(&afull[ab], aph, abrt, a.status) &&
-                            tc::mbar_wait(&efull[eb], aph, abrt, a.status);
+                            tc::mbar_wait(&efull[eb], eph, abrt, a.status);
             tc::tc_fence_after();
             uint8_t* e = epi + eb * kEBuf;
 #pragma unroll
@@ -608,6 +618,97 @@ __global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp,
 // R = sum of the split partials (fp32, pitch rp), R16 = bf16(R) (columns r..rp-1
 // zero), and per-chunk column sums of squares normpart[b][chunk][c] over rows
 // chunk*kRChunk ..: every sum in a fixed order, so results are reproducible.
+// ------------------------------------------------- wide ranks (rp > 256)
+// B = M + G as bf16 once, row-major (B16, pitch pb) and transposed (B16T,
+// pitch mp), for the two TMA GEMMs that replace the fused passes when the
+// rank spans several 256-column chunks (the fused passes would re-read M and
+// G once per chunk).  64 x 64 tiles; the transpose goes through shared memory.
+template <bool VEC>
+__global__ void __launch_bounds__(256) dion_formb_kernel(int m, int n, long long pb, long long mp, const float* M,
+                                                         const bf16* G, bf16* B16, bf16* B16T)
+{
+    __shared__ __align__(16) bf16 tile[64][72];
+    const int b = blockIdx.z, c0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
+    const size_t base = (size_t)b * m * n;
+    {
+        const int ri = threadIdx.x >> 2, cg = (threadIdx.x & 3) * 16, i = i0 + ri, c = c0 + cg;
+        float v[16];
+        if (VEC && i < m && c + 16 <= n) {
+            const float* mr = M + base + (size_t)i * n + c;
+            const bf16* gr = G + base + (size_t)i * n + c;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(mr + 4 * q));
+                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint4 g = __ldg(reinterpret_cast<const uint4*>(gr + 8 * q));
+                const bf16* h = reinterpret_cast<const bf16*>(&g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[8 * q + e] += __bfloat162float(h[e]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const size_t o = base + (size_t)i * n + c + e;
+                v[e] = (i < m && c + e < n) ? M[o] + __bfloat162float(G[o]) : 0.f;
+            }
+        }
+        uint4 w[2];
+        w[0] = make_uint4(tc::pack_bf16x2(v[0], v[1]), tc::pack_bf16x2(v[2], v[3]), tc::pack_bf16x2(v[4], v[5]),
+                          tc::pack_bf16x2(v[6], v[7]));
+        w[1] = make_uint4(tc::pack_bf16x2(v[8], v[9]), tc::pack_bf16x2(v[10], v[11]), tc::pack_bf16x2(v[12], v[13]),
+                          tc::pack_bf16x2(v[14], v[15]));
+        *reinterpret_cast<uint4*>(&tile[ri][cg]) = w[0];
+        *reinterpret_cast<uint4*>(&tile[ri][cg + 8]) = w[1];
+        if (i < m) {
+            bf16* o = B16 + (size_t)b * m * pb + (size_t)i * pb + c;
+            if (c + 16 <= n) {
+                *reinterpret_cast<uint4*>(o) = w[0];
+                *reinterpret_cast<uint4*>(o + 8) = w[1];
+            } else {
+                for (int e = 0; c + e < n && e < 16; ++e) o[e] = tile[ri][cg + e];
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const int cj = threadIdx.x >> 2, rg = (threadIdx.x & 3) * 16, c = c0 + cj, i = i0 + rg;
+        if (c < n) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                w[e] = (uint32_t)__bfloat16_as_ushort(tile[rg + 2 * e][cj]) |
+                       ((uint32_t)__bfloat16_as_ushort(tile[rg + 2 * e + 1][cj]) << 16);
+            bf16* o = B16T + (size_t)b * n * mp + (size_t)c * mp + i;
+            if (i + 16 <= m) {
+                *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+                for (int e = 0; i + e < m && e < 16; ++e) o[e] = tile[rg + e][cj];
+            }
+        }
+    }
+}
+
+// out[b] (cols x rows, pitch ldo) = in[b]^T (rows x cols, pitch ldi), bf16.
+__global__ void __launch_bounds__(256) dion_transpose16_kernel(int rows, int cols, long long ldi, long long si,
+                                                               long long ldo, long long so, const bf16* in, bf16* out)
+{
+    __shared__ bf16 tile[64][66];
+    const int b = blockIdx.z, c0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
+    for (int e = threadIdx.x; e < 64 * 64; e += 256) {
+        const int ri = e >> 6, cj = e & 63, i = i0 + ri, c = c0 + cj;
+        tile[ri][cj] = (i < rows && c < cols) ? in[(size_t)b * si + (size_t)i * ldi + c] : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 64 * 64; e += 256) {
+        const int cj = e >> 6, ri = e & 63, i = i0 + ri, c = c0 + cj;
+        if (i < rows && c < cols) out[(size_t)b * so + (size_t)c * ldo + i] = tile[ri][cj];
+    }
+}
+
 constexpr int kRChunk = 32;
 
 __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, int splits, int batch,
@@ -751,6 +852,40 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     // 1. Qt = bf16(Q^T)
     DION_TRY(launch("dion_prep_qt", dion_prep_qt_kernel, dim3((unsigned)cdiv(n, 32), (unsigned)cdiv(rp, 32), batch),
                     dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16));
+    const long long mp = (long long)align_up((size_t)m, 8);
+    if (L.wide) {
+        // 2'. B = M + G once in bf16 (and B^T); P = B Q as a TMA GEMM into part (one split)
+        bf16* B16 = (bf16*)(ws + L.B16);
+        bf16* B16T = (bf16*)(ws + L.B16T);
+        auto fk = vec ? dion_formb_kernel<true> : dion_formb_kernel<false>;
+        DION_TRY(launch("dion_formb", fk, dim3((unsigned)cdiv(n, 64), (unsigned)cdiv(m, 64), batch), dim3(256), 0, st, m,
+                        n, np, mp, (const float*)M, G, B16, B16T));
+        CUtensorMap tA, tB;
+        if (!make_tmap_3d(&tA, B16, TmapType::BF16, n, m, batch, np * 2, (long long)m * np * 2, 64, kBM) ||
+            !make_tmap_3d(&tB, Qt16, TmapType::BF16, n, rp, batch, np * 2, rp * np * 2, 64, 256))
+            return DION_ERR_CUDA;
+        TcGemmEpi e{};
+        e.M = m; e.N = rp; e.tiles_m = (int)cdiv(m, kBM); e.tiles_n = (int)cdiv(rp, 256); e.batch = batch;
+        e.Cf = part; e.ldc = rp; e.sc = (long long)m * rp; e.alpha = 0.f; e.beta = 1.f; e.status = status;
+        e.nseg = 1; e.zmul = 1;
+        DION_TRY(tc_gemm<256>("dion_bq_tc", tA, tB, n, e, st));
+        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, 1, P0, P1, P16, ws, L, status, st));
+        // 6'. R = B^T P: A = B^T (n x m), B = P^T (rp x m), both K-major
+        bf16* P16T = (bf16*)(ws + L.P16T);
+        DION_TRY(launch("dion_transpose_p", dion_transpose16_kernel,
+                        dim3((unsigned)cdiv(rp, 64), (unsigned)cdiv(m, 64), batch), dim3(256), 0, st, m, rp,
+                        (long long)rp, (long long)m * rp, mp, (long long)rp * mp, (const bf16*)P16, P16T));
+        CUtensorMap tA2, tB2;
+        if (!make_tmap_3d(&tA2, B16T, TmapType::BF16, m, n, batch, mp * 2, (long long)n * mp * 2, 64, kBM) ||
+            !make_tmap_3d(&tB2, P16T, TmapType::BF16, m, rp, batch, mp * 2, rp * mp * 2, 64, 256))
+            return DION_ERR_CUDA;
+        TcGemmEpi e2 = e;
+        e2.M = n; e2.tiles_m = (int)cdiv(n, kBM); e2.sc = (long long)n * rp;
+        DION_TRY(tc_gemm<256>("dion_btp_tc", tA2, tB2, m, e2, st));
+        const int nchunks = (int)cdiv(n, kRChunk);
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
+                        batch, (const float*)part, R, R16, normp));
+    } else {
     // 2. P partials = B Q
     CUtensorMap tmQt;
     if (!make_tmap_3d(&tmQt, Qt16, TmapType::BF16, n, rp, batch, np * 2, rp * np * 2, 64, nbox)) return DION_ERR_CUDA;
@@ -781,6 +916,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp,
                         splits, batch, (const float*)part, R, R16, normp));
     }
+    }
     {
         const int nchunks = (int)cdiv(n, kRChunk);
         DION_TRY(launch("dion_norm_final", dion_norm_final_kernel, dim3(batch), dim3(256), 0, st, r, rp, nchunks,
@@ -803,19 +939,30 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
             !make_tmap_3d(&tmG, G, TmapType::BF16, n, m, batch, (long long)n * 2, mn * 2, 64, kBM) ||
             !make_tmap_3d(&tmX, X, TmapType::BF16, n, m, batch, (long long)n * 2, mn * 2, 64, kBM))
             return DION_ERR_CUDA;
-        static bool pattr = false;
-        if (!pattr) {
-            DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kUpdPSmem));
-            pattr = true;
-        }
         const int tm = (int)cdiv(m, kBM), tn = (int)cdiv(n, kUBN);
         const long long tiles = (long long)tm * tn * batch;
         const int grid = (int)std::min<long long>(tiles, num_sms());
         UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n),
                     status};
-        DION_TRY(launch("dion_update_tc", dion_update_persist_kernel, dim3(grid), dim3(192), kUpdPSmem, st, tmPa, tmR,
-                        tmQ, tmM, tmG, tmX, ua));
+        if (ua.kchunks <= 4) {
+            static bool pattr = false;
+            if (!pattr) {
+                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<2, 2>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<2, 2>()));
+                pattr = true;
+            }
+            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<2, 2>, dim3(grid), dim3(192), upd_smem<2, 2>(),
+                            st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
+        } else {
+            static bool pattr_w = false;
+            if (!pattr_w) {
+                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<5, 1>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<5, 1>()));
+                pattr_w = true;
+            }
+            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<5, 1>, dim3(grid), dim3(192), upd_smem<5, 1>(),
+                            st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
+        }
     } else {
         static bool attr[2] = {false, false};
         auto k = vec ? dion_update_tc_kernel<true> : dion_update_tc_kernel<false>;

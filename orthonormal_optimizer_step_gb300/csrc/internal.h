@@ -12,11 +12,13 @@ struct DionLayout {
     int ksplit;             // splits of the B Q contraction over n (partials in Ppart)
     int ksplit_r;           // splits of the B^T P contraction over m
     size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Q16;
-    size_t T3, P3, Z3, S6;  // CholeskyQR2 operands of the tensor-core path
+    size_t P3, P3b, Z3, S6; // CholeskyQR2 operands of the tensor-core path (P3, P3b: bf16 terms of the panel)
     size_t normp;           // per-chunk column sums of squares of R
     size_t emax;            // per matrix max|S - I| of the second CholeskyQR Gram
     int nbc;                // block size of the blocked Cholesky (0: one CTA per matrix)
     size_t ZJ, A3;          // its diagonal-block inverse and panel terms
+    bool wide;              // rp > 256: B formed once in bf16 for both products
+    size_t B16, B16T, P16T; // bf16 B [m][round8(n)], B^T [n][round8(m)], P^T [rp][round8(m)]
     size_t total;
 };
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
@@ -42,6 +44,10 @@ struct CholIn {
     long long mstride, pstride;
     int lds;
     long long dstride;
+    // lds == 0 (factorization kernel for r <= 248, one partial only): the
+    // lower triangle is stored block-major, 8 x 8 block t = bi (bi + 1) / 2 + bj
+    // at Sin + b * mstride + 64 t, row-major inside the block (as written by
+    // qr_gram_sum_blocks)
 };
 // Cholesky + inverse of batch r x r Gram matrices (one CTA each); see qr.cu.
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,

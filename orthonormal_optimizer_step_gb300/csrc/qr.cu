@@ -379,12 +379,27 @@ __global__ void __launch_bounds__(512, 1) chol_gj_kernel(int r, const float* Sin
     for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) a[ii][jj] = 0.f;
+    if (in.lds == 0) {
+        // block-major input: this thread's 8 x 8 block is 64 contiguous floats
+        if (own) {
+            const float4* src = reinterpret_cast<const float4*>(Sb + (size_t)tid * 64);
+            float4 x[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) x[q] = __ldg(src + q);
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                a[ii][0] = x[2 * ii].x; a[ii][1] = x[2 * ii].y; a[ii][2] = x[2 * ii].z; a[ii][3] = x[2 * ii].w;
+                a[ii][4] = x[2 * ii + 1].x; a[ii][5] = x[2 * ii + 1].y; a[ii][6] = x[2 * ii + 1].z;
+                a[ii][7] = x[2 * ii + 1].w;
+            }
+        }
+    }
     // 4-column units: float4 loads when every row start is 16-byte aligned
     const bool vec = ((in.lds & 3) == 0) && ((in.pstride & 3) == 0) && ((in.mstride & 3) == 0) &&
                      (((uintptr_t)Sin & 15u) == 0);
     const int upr = cpad >> 2;   // units per staging row
     const int upr_round = kGjMaxParts / nparts;   // units loaded per round
-    for (int c = 0; c < cpad; c += kGjStageRows) {
+    for (int c = 0; c < (in.lds == 0 ? 0 : cpad); c += kGjStageRows) {
         const int rows = min(kGjStageRows, cpad - c), tot = rows * upr;
         // kGjMaxParts float4 loads in flight per thread: upr_round units of
         // nparts partials each (slot s = unit t * nparts + partial q)
@@ -618,7 +633,50 @@ __global__ void __launch_bounds__(512, 1) chol_gj_kernel(int r, const float* Sin
     const size_t zs = (size_t)r * ldz;
     bf16* z0 = W ? nullptr : Z3 + (size_t)3 * b * zs;
     float* Wo = W ? W + (size_t)b * r * r : nullptr;
-    for (int c = 0; c < r; c += kGjStageRows) {
+    if (!W && (ldz & 7) == 0) {
+        // straight from registers: each owner writes its block's three bf16
+        // terms (one 16-byte store per row and term); the blocks right of the
+        // diagonal blocks and the columns past them are written as zero
+        if (own) {
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                if (i0 + ii >= r) break;
+                uint32_t w[3][4];
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    uint32_t p1 = 0, p2 = 0, p3 = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float v = a[ii][t + h];
+                        const bf16 h1 = __float2bfloat16_rn(v);
+                        const float r1 = v - __bfloat162float(h1);
+                        const bf16 h2 = __float2bfloat16_rn(r1);
+                        const bf16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+                        p1 |= (uint32_t)__bfloat16_as_ushort(h1) << (16 * h);
+                        p2 |= (uint32_t)__bfloat16_as_ushort(h2) << (16 * h);
+                        p3 |= (uint32_t)__bfloat16_as_ushort(h3) << (16 * h);
+                    }
+                    w[0][t / 2] = p1;
+                    w[1][t / 2] = p2;
+                    w[2][t / 2] = p3;
+                }
+                bf16* o = z0 + (size_t)(i0 + ii) * ldz + j0;
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    *reinterpret_cast<uint4*>(o + q * zs) = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+            }
+        }
+        const int upr8 = ldz >> 3, tot = r * upr8;
+        for (int e = tid; e < tot; e += nt) {
+            const int i = e / upr8, jb = e - i * upr8;
+            if (jb > (i >> 3)) {
+                bf16* o = z0 + (size_t)i * ldz + jb * 8;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) *reinterpret_cast<uint4*>(o + q * zs) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    for (int c = 0; c < ((!W && (ldz & 7) == 0) ? 0 : r); c += kGjStageRows) {
         const int rows = min(kGjStageRows, r - c);
         if (own && i0 >= c && i0 < c + rows) {
 #pragma unroll
@@ -709,6 +767,7 @@ cudaError_t chol_inv_io(const char* name, int batch, int r, const float* Sin, in
                         float* W, bf16* Z3, int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre,
                         CholIn in)
 {
+    if (in.lds == 0 && (r > kGjMaxR || nparts != 1)) return cudaErrorInvalidValue;   // block-major input
     if (r <= kGjMaxR) {
         if (nparts < 1 || nparts > kGjMaxParts) return cudaErrorInvalidValue;
         static bool gj_attr = false;

@@ -8,8 +8,11 @@
 // whose weight is at least 2^-16:
 //     X Y ~ X1Y1 + X1Y2 + X1Y3 + X2Y1 + X2Y2 + X3Y1
 // The GEMM walks these as six K segments that pick the split of each operand.
-// The Gram runs the segments as six separate partial products (more CTAs on
-// the small r x r output); the factorization kernel sums them on load.
+// The Gram reads the terms of the row-major m x r panel MN-major (no
+// transposed copy) and runs the segments as six separate partial products
+// (more CTAs on the small r x r output), summed afterwards.  Only the first
+// pass splits a float32 panel: its apply writes the terms of its result
+// directly for the second pass.
 #include <algorithm>
 
 #include "internal.h"
@@ -32,46 +35,52 @@ __device__ __forceinline__ void split3(float v, bf16& h1, bf16& h2, bf16& h3)
     h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
 }
 
-// P (m x rp fp32, pitch rp) -> P3[3b + t] (m x rp, natural) and T3[3b + t]
-// (rp x mp, transposed), t = 0, 1, 2 the three bf16 terms; columns r..rp-1
-// are written as zero.  P may be given as nparts split partials (summed here,
-// pitch pstride); Pf, if set, receives the float32 sum (pitch rp).
-__global__ void __launch_bounds__(256) qr_split_kernel(int m, int r, int rp, int mp, const float* P, int nparts,
-                                                       long long pstride, bf16* P3, bf16* T3, float* Pf)
+// P (m x rp fp32, pitch rp) -> P3[3b + t] (m x rp), t = 0, 1, 2 the three
+// bf16 terms; columns r..rp-1 are written as zero.  P may be given as nparts
+// split partials (summed here, pitch pstride); Pf, if set, receives the
+// float32 sum (pitch rp).  One thread per 4 columns.
+__global__ void __launch_bounds__(256) qr_split_kernel(int m, int r, int rp, const float* P, int nparts,
+                                                       long long pstride, bf16* P3, float* Pf, long long total4)
 {
-    __shared__ float tile[32][33];
-    const int b = blockIdx.z, c0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
-    const size_t pn = (size_t)m * rp, tn = (size_t)rp * mp;
-    for (int ii = threadIdx.y; ii < 32; ii += 8) {
-        const int i = i0 + ii, c = c0 + threadIdx.x;
-        float v = 0.f;
-        if (i < m && c < rp) {
-            const size_t o = (size_t)b * pn + (size_t)i * rp + c;
-            if (c < r) {
-                v = P[o];
-                for (int q = 1; q < nparts; ++q) v += P[o + q * pstride];
+    const int b = blockIdx.y;
+    const size_t pn = (size_t)m * rp;
+    const int upr = rp >> 2;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total4;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(e / upr), c = (int)(e - (long long)i * upr) * 4;
+        const size_t o = (size_t)b * pn + (size_t)i * rp + c;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < r) {
+            v = *reinterpret_cast<const float4*>(P + o);
+            for (int q = 1; q < nparts; ++q) {
+                const float4 u = *reinterpret_cast<const float4*>(P + o + q * pstride);
+                v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
             }
-            if (Pf) Pf[o] = v;
-            bf16 h1, h2, h3;
-            split3(v, h1, h2, h3);
-            bf16* po = P3 + (size_t)3 * b * pn + (size_t)i * rp + c;
-            po[0] = h1;
-            po[pn] = h2;
-            po[2 * pn] = h3;
+            if (c + 1 >= r) v.y = 0.f;
+            if (c + 2 >= r) v.z = 0.f;
+            if (c + 3 >= r) v.w = 0.f;
         }
-        tile[ii][threadIdx.x] = v;
-    }
-    __syncthreads();
-    for (int cc = threadIdx.y; cc < 32; cc += 8) {
-        const int c = c0 + cc, i = i0 + threadIdx.x;
-        if (i < m && c < rp) {
-            bf16 h1, h2, h3;
-            split3(tile[threadIdx.x][cc], h1, h2, h3);
-            bf16* o = T3 + (size_t)3 * b * tn + (size_t)c * mp + i;
-            o[0] = h1;
-            o[tn] = h2;
-            o[2 * tn] = h3;
+        if (Pf) *reinterpret_cast<float4*>(Pf + o) = v;
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w[3][2];
+#pragma unroll
+        for (int t = 0; t < 4; t += 2) {
+            uint32_t p1 = 0, p2 = 0, p3 = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                bf16 h1, h2, h3;
+                split3(x[t + h], h1, h2, h3);
+                p1 |= (uint32_t)__bfloat16_as_ushort(h1) << (16 * h);
+                p2 |= (uint32_t)__bfloat16_as_ushort(h2) << (16 * h);
+                p3 |= (uint32_t)__bfloat16_as_ushort(h3) << (16 * h);
+            }
+            w[0][t / 2] = p1;
+            w[1][t / 2] = p2;
+            w[2][t / 2] = p3;
         }
+        bf16* po = P3 + (size_t)3 * b * pn + (size_t)i * rp + c;
+#pragma unroll
+        for (int t = 0; t < 3; ++t) *reinterpret_cast<uint2*>(po + t * pn) = make_uint2(w[t][0], w[t][1]);
     }
 }
 
@@ -144,6 +153,43 @@ __global__ void __launch_bounds__(256) qr_sum_kernel(long long rr, int nparts, c
     }
 }
 
+// S[b] = sum of the nparts partial Grams, written block-major for the
+// one-CTA factorization: the lower triangle in 8 x 8 blocks t = bi (bi + 1)/2
+// + bj, 64 contiguous floats each (row-major inside the block); the strict
+// upper part of a diagonal block is zero and rows beyond r are the identity.
+__global__ void __launch_bounds__(256) qr_sum_blocks_kernel(int r, int nparts, const float* __restrict__ S6,
+                                                            float* __restrict__ Sblk, long long sblk)
+{
+    const int b = blockIdx.y;
+    const int nbr = (r + 7) >> 3;
+    const long long tot4 = (long long)nbr * (nbr + 1) / 2 * 16;   // float4 units
+    const size_t rr = (size_t)r * r;
+    const float* src = S6 + (size_t)b * nparts * rr;
+    float* dst = Sblk + (size_t)b * sblk;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < tot4;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(e >> 4), q = (int)(e & 15), ii = q >> 1, j0 = (q & 1) * 4;
+        int bi = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
+        while ((bi + 1) * (bi + 2) / 2 <= t) ++bi;
+        while (bi * (bi + 1) / 2 > t) --bi;
+        const int bj = t - bi * (bi + 1) / 2;
+        const int i = bi * 8 + ii, j = bj * 8 + j0;
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int jj = j + u;
+            float x = (i == jj && i >= r) ? 1.f : 0.f;
+            if (i < r && jj <= i) {
+                const size_t o = (size_t)i * r + jj;
+                x = src[o];
+                for (int p = 1; p < nparts; ++p) x += src[p * rr + o];
+            }
+            v[u] = x;
+        }
+        reinterpret_cast<float4*>(dst)[e] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 // Panel of the blocked factorization: rows x w block of S (pitch r, matrix
 // pitch r*r) -> three bf16 terms A3[3b + t] (rows x nb, pitch nb, term pitch
 // r*nb), columns w..nb-1 zero.
@@ -174,6 +220,16 @@ constexpr int kCholOneCtaMaxR = 248;
 constexpr int kCholBlock = 128;
 
 int pick_bn_qr(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 192 ? 192 : 256)); }
+
+// Both operands MN-major (the Gram of a row-major panel).
+cudaError_t gemm_mn(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
+                    cudaStream_t st)
+{
+    if (bn == 64) return tc_gemm<64, true>(name, ta, tb, K, ep, st);
+    if (bn == 128) return tc_gemm<128, true>(name, ta, tb, K, ep, st);
+    if (bn == 192) return tc_gemm<192, true>(name, ta, tb, K, ep, st);
+    return tc_gemm<256, true>(name, ta, tb, K, ep, st);
+}
 
 cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
                      cudaStream_t st)
@@ -220,11 +276,12 @@ TcGemmEpi six_term_epi(int M, int N, int bn, int batch, int* status, const int* 
 //   X_J  = Y_J Z_JJ^T                ... and the diagonal block
 // All products are six-term split GEMMs (float32 accuracy).  L lives only as
 // its three bf16 terms in L3 (r x rp, pitch rp); the terms of X and Y replace
-// those of P in P3 column block by column block.  Matrices whose gate entry is
-// at most kNearIdentityTol are skipped by every kernel.
+// those of P in P3 column block by column block (with keep_terms, P3 ends as
+// the terms of X).  Matrices whose gate entry is at most kNearIdentityTol are
+// skipped by every kernel.
 cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const float* Psrc, float* dst, bf16* P16,
                                float* S, float* W, bf16* ZJ, bf16* A3, bf16* L3, bf16* P3, int* dead, int* status,
-                               const int* gate, cudaStream_t st)
+                               const int* gate, bool keep_terms, cudaStream_t st)
 {
     const int nblk = (int)cdiv(r, nb);
     const long long z3 = 3ll * batch, rr = (long long)r * r, mrp = (long long)m * rp, rrp = (long long)r * rp;
@@ -292,7 +349,7 @@ cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const fl
         e2.C = P16 ? P16 + j0 : nullptr;
         e2.ldc = rp;
         e2.sc = mrp;
-        if (J + 1 < nblk) {
+        if (J + 1 < nblk || keep_terms) {   // the terms of X feed later blocks (and the second pass)
             e2.Cs3 = P3 + j0;
             e2.ldcs3 = rp;
             e2.scs3 = mrp;
@@ -310,50 +367,62 @@ int chol_block_size(int r) { return r > kCholOneCtaMaxR ? kCholBlock : 0; }
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st)
 {
-    bf16* T3 = (bf16*)(ws + L.T3);
     bf16* P3 = (bf16*)(ws + L.P3);
+    bf16* P3b = (bf16*)(ws + L.P3b);
     bf16* Z3 = (bf16*)(ws + L.Z3);
     float* S6 = (float*)(ws + L.S6);
     float* S = (float*)(ws + L.S);
     float* W = (float*)(ws + L.W);
     int* dead = (int*)(ws + L.dead);
     int* emax = (int*)(ws + L.emax);
-    const long long mp = (long long)align_up((size_t)m, 8);
     const int bn = pick_bn_qr(r), bna = pick_bn_qr(rp);
     const bool blocked = L.nbc > 0;
     // blocked: the Gram's lower half, accumulated straight into S when that
     // alone fills the SMs, else as six partials summed afterwards
     const bool direct = blocked && cdiv(r, 128) * cdiv(r, bn) * batch / 2 >= num_sms();
 
-    CUtensorMap tTa, tTb, tPa, tZb;
-    if (!make_tmap_3d(&tTa, T3, TmapType::BF16, m, rp, 3ll * batch, mp * 2, (long long)rp * mp * 2, 64, 128) ||
-        !make_tmap_3d(&tTb, T3, TmapType::BF16, m, rp, 3ll * batch, mp * 2, (long long)rp * mp * 2, 64, bn) ||
-        !make_tmap_3d(&tPa, P3, TmapType::BF16, rp, m, 3ll * batch, (long long)rp * 2, (long long)m * rp * 2, 64, 128) ||
-        !make_tmap_3d(&tZb, Z3, TmapType::BF16, rp, r, 3ll * batch, (long long)rp * 2, (long long)r * rp * 2, 64, bna))
+    // The bf16 terms of the panel: P3 holds those of the first pass's input;
+    // the second pass reads those of its input from P3b (written by the
+    // first apply) or, on the blocked path, from P3 (rewritten in place by the
+    // blocked solve).  The Gram reads them MN-major (64 x 64 boxes), the apply
+    // K-major (64 x 128).
+    const long long pz = (long long)m * rp * 2;
+    CUtensorMap tG[2], tPa[2], tZb;
+    for (int t = 0; t < 2; ++t) {
+        bf16* base = t == 0 ? P3 : P3b;
+        if (!make_tmap_3d(&tG[t], base, TmapType::BF16, rp, m, 3ll * batch, (long long)rp * 2, pz, 64, 64) ||
+            !make_tmap_3d(&tPa[t], base, TmapType::BF16, rp, m, 3ll * batch, (long long)rp * 2, pz, 64, 128))
+            return cudaErrorInvalidValue;
+    }
+    if (!make_tmap_3d(&tZb, Z3, TmapType::BF16, rp, r, 3ll * batch, (long long)rp * 2, (long long)r * rp * 2, 64, bna))
         return cudaErrorInvalidValue;
 
     // pass 1: split partials of P -> Ptmp;  pass 2: Ptmp -> P (and P16)
     for (int pass = 0; pass < 2; ++pass) {
         const float* src = pass == 0 ? Pin : Ptmp;
         float* dst = pass == 0 ? Ptmp : P;
-        const int np_ = pass == 0 ? nparts : 1;
-        cudaError_t e = launch("qr_split", qr_split_kernel, dim3((unsigned)cdiv(rp, 32), (unsigned)cdiv(m, 32), batch),
-                               dim3(32, 8), 0, st, m, r, rp, (int)mp, src, np_, (long long)batch * m * rp, P3, T3,
-                               (blocked && pass == 0) ? dst : (float*)nullptr);
-        if (e != cudaSuccess) return e;
+        const int ti = (pass == 1 && !blocked) ? 1 : 0;   // which terms hold this pass's input
+        cudaError_t e = cudaSuccess;
+        if (pass == 0) {
+            const long long total4 = (long long)m * (rp / 4);
+            e = launch("qr_split", qr_split_kernel, dim3((unsigned)std::min<long long>(cdiv(total4, 256), 2048), batch),
+                       dim3(256), 0, st, m, r, rp, src, nparts, (long long)batch * m * rp, P3,
+                       blocked ? dst : (float*)nullptr, total4);
+            if (e != cudaSuccess) return e;
+        }
         if (direct) {
             TcGemmEpi eg = six_term_epi(r, r, bn, batch, status, nullptr);
             eg.Cf = S;
             eg.ldc = r;
             eg.sc = (long long)r * r;
             eg.lower = 1;
-            e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
+            e = gemm_mn(bn, "qr_gram_tc", tG[ti], tG[ti], m, eg, st);
         } else {
             // six partial Grams S6[6b + q] = T_a(q) T_b(q)^T  (r x r)
             TcGemmEpi eg{r, r, (int)cdiv(r, 128), (int)cdiv(r, bn), 6 * batch, nullptr, r, (long long)r * r,
                          nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, S6, 6, 3, 1, kSelA, kSelB};
             eg.lower = blocked ? 1 : 0;
-            e = gemm_any(bn, "qr_gram_tc", tTa, tTb, m, eg, st);
+            e = gemm_mn(bn, "qr_gram_tc", tG[ti], tG[ti], m, eg, st);
         }
         if (e != cudaSuccess) return e;
         if (pass == 1) {
@@ -372,20 +441,31 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
             // factorization reads one matrix; the second pass factors only
             // matrices that failed the near-identity test and reads the partials
             if (pass == 0) {
-                const long long rr = (long long)r * r;
-                e = launch("qr_gram_sum", qr_sum_kernel, dim3((unsigned)std::min<long long>(cdiv(rr, 1024), 1024), batch),
-                           dim3(256), 0, st, rr, 6, (const float*)S6, S, (const int*)nullptr);
+                const long long nb8 = (r + 7) / 8, sblk = nb8 * (nb8 + 1) / 2 * 64;
+                e = launch("qr_gram_sum", qr_sum_blocks_kernel,
+                           dim3((unsigned)std::min<long long>(cdiv(sblk / 4, 256), 1024), batch), dim3(256), 0, st, r, 6,
+                           (const float*)S6, S, sblk);
                 if (e != cudaSuccess) return e;
+                e = chol_inv_io("chol_inv_pass1", batch, r, S, 1, S, W, nullptr, Z3, rp, dead, status, st, nullptr,
+                                CholIn{sblk, 0, 0, r});
+            } else {
+                e = chol_inv("chol_inv_pass2", batch, r, S6, 6, S, W, nullptr, Z3, rp, dead, status, st, gate);
             }
-            e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, pass == 0 ? S : S6, pass == 0 ? 1 : 6,
-                         S, W, nullptr, Z3, rp, dead, status, st, gate);
             if (e != cudaSuccess) return e;
         }
         if (!blocked || pass == 1) {
-            // dst = P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out zero
+            // P L^{-T}: all six cross terms accumulated; columns r..rp-1 come out
+            // zero.  First pass: only its bf16 terms (P3b) for the second pass;
+            // second pass: P (float32) and P16.
             TcGemmEpi ea{m, rp, (int)cdiv(m, 128), (int)cdiv(rp, bna), batch, pass == 1 ? P16 : nullptr, rp,
-                         (long long)m * rp, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, dst, 6, 3, 0, kSelA, kSelB};
-            e = gemm_any(bna, "qr_apply_tc", tPa, tZb, rp, ea, st);
+                         (long long)m * rp, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, pass == 1 ? dst : nullptr,
+                         6, 3, 0, kSelA, kSelB};
+            if (pass == 0) {
+                ea.Cs3 = P3b;
+                ea.ldcs3 = rp;
+                ea.scs3 = (long long)m * rp;
+            }
+            e = gemm_any(bna, "qr_apply_tc", tPa[ti], tZb, rp, ea, st);
             if (e != cudaSuccess) return e;
         }
         if (blocked) {
@@ -396,7 +476,7 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                 if (e != cudaSuccess) return e;
             }
             e = chol_blocked_apply(batch, m, r, rp, L.nbc, pass == 0 ? dst : src, dst, pass == 1 ? P16 : nullptr, S, W,
-                                   (bf16*)(ws + L.ZJ), (bf16*)(ws + L.A3), Z3, P3, dead, status, gate, st);
+                                   (bf16*)(ws + L.ZJ), (bf16*)(ws + L.A3), Z3, P3, dead, status, gate, pass == 0, st);
             if (e != cudaSuccess) return e;
         }
     }

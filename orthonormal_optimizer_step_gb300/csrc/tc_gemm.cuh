@@ -179,7 +179,11 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
     }
 }
 
-template <int BN>
+// MN = true: both operands are MN-major (the M or N index contiguous, K
+// rows): tmA and tmB have 64 x 64 boxes (MN x K) landing as 64-wide MN blocks
+// of the 128-byte swizzle (8 KB apart), so a row-major m x r panel serves as
+// the operand of its own Gram matrix without a transposed copy.
+template <int BN, bool MN = false>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int K, TcGemmEpi ep)
 {
@@ -238,8 +242,19 @@ __global__ void __launch_bounds__(192, 1)
                         if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) break;
                         uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
                         tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                        tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
-                        tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
+                        if (MN) {
+#pragma unroll
+                            for (int blk = 0; blk < Cfg::BM / 64; ++blk)
+                                tc::tma_load_3d(sa + blk * 8192, &tmA, &full[stage], tm * Cfg::BM + blk * 64,
+                                                kc * Cfg::BK, za);
+#pragma unroll
+                            for (int blk = 0; blk < BN / 64; ++blk)
+                                tc::tma_load_3d(sa + Cfg::A_BYTES + blk * 8192, &tmB, &full[stage], tn * BN + blk * 64,
+                                                kc * Cfg::BK, zb);
+                        } else {
+                            tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
+                            tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
+                        }
                         if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
                     }
                 }
@@ -247,7 +262,7 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::make_idesc(Cfg::BM, BN, 1, false, false);
+            constexpr uint32_t idesc = tc::make_idesc(Cfg::BM, BN, 1, MN, MN);
             int stage = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -269,9 +284,14 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t a0 = tc::smem_u32(smem + stage * Cfg::STAGE_BYTES);
                     const uint32_t b0 = a0 + Cfg::A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k)
-                        tc::mma_bf16(d, tc::make_sdesc(a0 + k * 32, 16, 1024), tc::make_sdesc(b0 + k * 32, 16, 1024),
-                                     idesc, (kc | k) != 0);
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {
+                        if (MN)
+                            tc::mma_bf16(d, tc::make_sdesc(a0 + k * 2048, 8192, 1024),
+                                         tc::make_sdesc(b0 + k * 2048, 8192, 1024), idesc, (kc | k) != 0);
+                        else
+                            tc::mma_bf16(d, tc::make_sdesc(a0 + k * 32, 16, 1024), tc::make_sdesc(b0 + k * 32, 16, 1024),
+                                         idesc, (kc | k) != 0);
+                    }
                     tc::mma_commit(&empty[stage]);
                     if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
                 }
@@ -313,22 +333,23 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-// Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN.
-template <int BN>
+// Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN
+// (MN: both 64 x 64, MN x K).
+template <int BN, bool MN = false>
 cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
                     cudaStream_t st)
 {
     using Cfg = TcGemmCfg<BN>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Cfg::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int tiles = ep.batch * ep.tiles_m * ep.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    return launch(name, tc_gemm_kernel<BN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
+    return launch(name, tc_gemm_kernel<BN, MN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
 }
 
 }  // namespace
