@@ -60,6 +60,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.Z3 = carve(off, 3 * b * r * rp * h);
         L.S6 = carve(off, 6 * b * r * r * f);
         L.normp = carve(off, b * (size_t)cdiv(n, 32) * rp * f);
+        L.rcount = carve(off, b * sizeof(int));
         L.emax = carve(off, b * sizeof(int));
         if (L.wide) {
             const size_t mp = align_up((size_t)m, 8), np = align_up((size_t)n, 8);
@@ -82,7 +83,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.wide = false;
         L.ZJ = L.A3 = L.B16 = L.B16T = L.P16T = off;
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
-        L.P3 = L.P3b = L.Z3 = L.S6 = L.normp = L.emax = off;
+        L.P3 = L.P3b = L.Z3 = L.S6 = L.normp = L.rcount = L.emax = off;
     }
     L.total = off;
     return L;
@@ -179,6 +180,8 @@ extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dt
     if (!aligned16(X) || !aligned16(G) || !aligned16(M) || !aligned16(Q)) return DION_ERR_INVALID_ARG;
     if (!std::isfinite(mu) || !std::isfinite(lr) || !std::isfinite(weight_decay)) return DION_ERR_INVALID_ARG;
     const DionLayout L = dion_layout(batch, m, n, r, dt);
+    // the tensor-core path addresses the batch x n x rp panel of R in 4-column units with 32-bit indices
+    if (L.tc && (long long)batch * n * (L.rp / 4) >= (1ll << 31)) return DION_ERR_UNSUPPORTED;
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)cuda_stream;
     if (L.tc) return dion_step_tc(batch, m, n, r, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);

@@ -12,8 +12,9 @@
 //   6. dion_btp_tc   : R = B^T P, contracting over m: both operands are read
 //                      MN-major (B rows are K rows), so B is again formed in
 //                      registers without any transpose; split over m
-//   7. dion_rsum     : R = sum of partials, R16 = bf16(R), partial column norms
-//   8. dion_norm_final, dion_qemit: Q = R / ||R_j|| (caller's fp32 Q) and Q16
+//   7. dion_rsum     : R = sum of partials, R16 = bf16(R), column norms (the
+//                      last CTA of each matrix finishes them)
+//   8. dion_qemit    : Q = R / ||R_j|| (caller's fp32 Q) and Q16
 //   9. dion_update_tc: per 128 x 64 tile, two accumulators P R^T and P Q^T in
 //                      tensor memory; the epilogue streams M, G, X once:
 //                      M <- M + G - (1-mu) P R^T,  X <- (1-lr wd) X - lr sqrt(m/n) P Q^T
@@ -100,7 +101,7 @@ __device__ __forceinline__ uint4 sum_pack8(const Raw8& r)
 
 struct PassArgs {
     int m, n, rp, batch;
-    int rchunks;            // r-chunks of 256 columns
+    int splits;             // K splits (fp32 partial planes)
     int kchunks_per_split;  // 64-wide K chunks per split
     int kchunks;            // total K chunks
     const float* M;
@@ -109,18 +110,27 @@ struct PassArgs {
     int* status;
 };
 
-constexpr int kProducers = 512;   // 16 producer warps; warp 16 issues the MMAs
-constexpr int kPassWarps = kProducers / 32 + 1;
-constexpr int kPerProducer = 1024 / kProducers;   // 8-element groups of a 128 x 64 tile per producer thread
+constexpr int kProducers = 512;                  // warps 0..15 build the B tiles
+constexpr int kMmaWarp = kProducers / 32;        // warp 16 issues the MMAs
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 17..20 drain the accumulators
+constexpr int kPassWarps = kEpiWarp0 + 4;
+constexpr int kPerProducer = 1024 / kProducers;  // 8-element groups of a 128 x 64 tile per producer thread
 constexpr int kStages = 4;
 constexpr uint32_t kAB = kBM * kBK * 2;          // 16 KB bf16 A tile
 constexpr uint32_t kBB = 256 * kBK * 2;          // up to 32 KB B tile
 constexpr uint32_t kStage = kAB + kBB;
 constexpr size_t kPassSmem = (size_t)kStages * kStage + 1024 + 256;
 
-// Shared skeleton of the two streaming passes.  MN_A = false: pass 2 (P = B Q),
-// A tile = 128 rows of B x 64 columns, K-major.  MN_A = true: pass 6
-// (R = B^T P), A tile = 64 rows of B x 128 columns, MN-major.
+// The two streaming passes (rp <= 256; wider ranks use the TMA GEMMs), as a
+// persistent kernel over work units (batch entry, K split, 128-row output
+// tile; tiles fastest, so concurrent CTAs share the operand chunks in L2).
+// MN_A = false: P = B Q, A tile = 128 rows of B x 64 columns, K-major.
+// MN_A = true:  R = B^T P, A tile = 64 rows of B x 128 columns, MN-major.
+// Producer warps form B = M + G in registers (two chunks of loads in flight,
+// across unit boundaries), round to bf16 and write the swizzled A tile; one
+// thread adds the operand tile (Q^T or P) by TMA.  The accumulator is double
+// buffered in tensor memory, so the epilogue warps write the fp32 partials of
+// one unit while the next unit streams.
 template <bool MN_A, bool VEC>
 __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB, PassArgs a)
 {
@@ -128,33 +138,40 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + kStages * kStage);
     uint64_t* empty = full + kStages;
-    uint64_t* done = empty + kStages;
-    uint32_t* tmem_slot = (uint32_t*)(done + 1);
+    uint64_t* acc_full = empty + kStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
     int* abort_flag = (int*)(tmem_slot + 1);
     volatile int* abrt = abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int tile = blockIdx.x;                       // 128-wide output row tile
-    const int rc = blockIdx.y % a.rchunks, split = blockIdx.y / a.rchunks;
-    const int b = blockIdx.z;
-    const int nN = min(256, a.rp - rc * 256);          // MMA N (multiple of 64)
-    const int nbox = min(256, a.rp);                   // rows (or columns) of one B box
-    const int kc0 = split * a.kchunks_per_split;
-    const int nk = min(a.kchunks_per_split, a.kchunks - kc0);
     const int out_rows = MN_A ? a.n : a.m;
-    const uint32_t b_bytes = MN_A ? (uint32_t)((nbox + 63) / 64) * 8192u : (uint32_t)nbox * 128u;
+    const int tiles = (out_rows + kBM - 1) / kBM;
+    const int units = tiles * a.splits * a.batch;
+    const int nN = a.rp;                               // MMA N (multiple of 64, at most 256)
+    const uint32_t b_bytes = MN_A ? (uint32_t)(nN / 64) * 8192u : (uint32_t)nN * 128u;
+    auto unit_of = [&](int u, int& b, int& split, int& tile, int& kc0, int& nk) {
+        tile = u % tiles;
+        split = (u / tiles) % a.splits;
+        b = u / (tiles * a.splits);
+        kc0 = split * a.kchunks_per_split;
+        nk = min(a.kchunks_per_split, a.kchunks - kc0);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(&full[s], kProducers / 32 + 1);   // one arrive per producer warp + the TMA
             tc::mbar_init(&empty[s], 1);
         }
-        tc::mbar_init(done, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&acc_full[s], 1);
+            tc::mbar_init(&acc_empty[s], 4);
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    if (warp == kPassWarps - 1) {
-        tc::tmem_alloc(tmem_slot, 256);
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
@@ -162,37 +179,47 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < kPassWarps - 1) {
-        // ---------------- producers: B = M + G -> bf16 -> swizzled A tile.
-        // The global loads of chunks kc + 1 and kc + 2 are issued before chunk
-        // kc is converted and stored, so three chunks of loads are in flight.
-        Raw8 cur[kPerProducer], nxt[kPerProducer], nxt2[kPerProducer];
+    if (warp < kMmaWarp) {
+        // ---------------- producers: B = M + G -> bf16 -> swizzled A tile
+        Raw8 cur[kPerProducer], nxt[kPerProducer];
         uint32_t off[kPerProducer];
-        auto fetch = [&](int kc, Raw8 (&dst)[kPerProducer]) {
-            const int k0 = (kc0 + kc) * kBK;
+        auto fetch = [&](int b, int tile, int kc, Raw8 (&dst)[kPerProducer]) {
+            const int k0 = kc * kBK;
 #pragma unroll
-            for (int u = 0; u < kPerProducer; ++u) {
-                const int g = threadIdx.x + kProducers * u;
+            for (int v = 0; v < kPerProducer; ++v) {
+                const int g = threadIdx.x + kProducers * v;
                 if (!MN_A) {
                     const int row = g >> 3, ch = g & 7;             // 128 rows x 8 chunks
                     const int i = tile * kBM + row;
-                    fetch_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, k0 + ch * 8, a.n, dst[u]);
-                    off[u] = tc::sw128_offset(row, ch);
+                    fetch_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, k0 + ch * 8, a.n, dst[v]);
+                    off[v] = tc::sw128_offset(row, ch);
                 } else {
                     const int row = g >> 4, ch = g & 15;            // 64 K-rows x 16 chunks
                     const int i = k0 + row;
                     fetch_b8<VEC>(a.M, a.G, ((long long)b * a.m + i) * a.n, i, a.m, tile * kBM + ch * 8, a.n,
-                                  dst[u]);
-                    off[u] = (ch >> 3) * 8192u + tc::sw128_offset(row, ch & 7);
+                                  dst[v]);
+                    off[v] = (ch >> 3) * 8192u + tc::sw128_offset(row, ch & 7);
                 }
             }
         };
-        if (nk > 0) fetch(0, cur);
-        if (nk > 1) fetch(1, nxt);
-        for (int kc = 0; kc < nk && !*abrt; ++kc) {
-            if (kc + 2 < nk) fetch(kc + 2, nxt2);
-            const int stage = kc % kStages;
-            const uint32_t ph = (kc / kStages) & 1;
+        // cursor over the flattened (unit, chunk) sequence of this CTA
+        int u = blockIdx.x, b = 0, split = 0, tile = 0, kc0 = 0, nk = 0, kc = 0;
+        if (u < units) unit_of(u, b, split, tile, kc0, nk);
+        int nu = u, nb = b, ntile = tile, nkc0 = kc0, nnk = nk, nkc = 0;   // the chunk after the current one
+        auto advance = [&]() {
+            if (++nkc >= nnk) {
+                nu += gridDim.x;
+                nkc = 0;
+                int sp;
+                if (nu < units) unit_of(nu, nb, sp, ntile, nkc0, nnk);
+            }
+        };
+        if (u < units) fetch(b, tile, kc0, cur);
+        advance();
+        int stage = 0;
+        uint32_t ph = 0;
+        while (u < units && !*abrt) {
+            if (nu < units) fetch(nb, ntile, nkc0 + nkc, nxt);
             if (lane == 0) tc::mbar_wait(&empty[stage], ph ^ 1, abrt, a.status);
             __syncwarp();
             if (*abrt) break;
@@ -201,73 +228,93 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
             if (threadIdx.x == 0) {
                 tc::mbar_arrive_expect_tx(&full[stage], b_bytes);
                 if (MN_A) {
-                    for (int blk = 0; blk * 64 < nbox; ++blk)
-                        tc::tma_load_3d(sA + kAB + blk * 8192, &tmB, &full[stage], rc * 256 + blk * 64, k0, b);
+                    for (int blk = 0; blk * 64 < nN; ++blk)
+                        tc::tma_load_3d(sA + kAB + blk * 8192, &tmB, &full[stage], blk * 64, k0, b);
                 } else {
-                    tc::tma_load_3d(sA + kAB, &tmB, &full[stage], k0, rc * 256, b);
+                    tc::tma_load_3d(sA + kAB, &tmB, &full[stage], k0, 0, b);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kPerProducer; ++u) *reinterpret_cast<uint4*>(sA + off[u]) = sum_pack8(cur[u]);
+            for (int v = 0; v < kPerProducer; ++v) *reinterpret_cast<uint4*>(sA + off[v]) = sum_pack8(cur[v]);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&full[stage]);
+            if (++stage == kStages) { stage = 0; ph ^= 1; }
 #pragma unroll
-            for (int u = 0; u < kPerProducer; ++u) {
-                cur[u] = nxt[u];
-                nxt[u] = nxt2[u];
-            }
+            for (int v = 0; v < kPerProducer; ++v) cur[v] = nxt[v];
+            u = nu; b = nb; tile = ntile; kc0 = nkc0; nk = nnk; kc = nkc;
+            advance();
         }
-    } else if (lane == 0) {
-        // ---------------- MMA issuer
-        const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, MN_A);
-        for (int kc = 0; kc < nk; ++kc) {
-            const int stage = kc % kStages;
-            const uint32_t ph = (kc / kStages) & 1;
-            if (!tc::mbar_wait(&full[stage], ph, abrt, a.status)) break;
-            tc::tc_fence_after();
-            const uint32_t a0 = tc::smem_u32(smem + stage * kStage), b0 = a0 + kAB;
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, MN_A);
+            int stage = 0, it = 0;
+            uint32_t ph = 0;
+            for (int u = blockIdx.x; u < units && !*abrt; u += gridDim.x, ++it) {
+                int b, split, tile, kc0, nk;
+                unit_of(u, b, split, tile, kc0, nk);
+                const int buf = it & 1;
+                if (!tc::mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1, abrt, a.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + buf * 256;
+                bool ok = true;
+                for (int kc = 0; kc < nk; ++kc) {
+                    if (!tc::mbar_wait(&full[stage], ph, abrt, a.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(smem + stage * kStage), b0 = a0 + kAB;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-                uint64_t ad, bd;
-                if (MN_A) {
-                    ad = tc::make_sdesc(a0 + k * 2048, 8192, 1024);
-                    bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
-                } else {
-                    ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
-                    bd = tc::make_sdesc(b0 + k * 32, 16, 1024);
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        uint64_t ad, bd;
+                        if (MN_A) {
+                            ad = tc::make_sdesc(a0 + k * 2048, 8192, 1024);
+                            bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
+                        } else {
+                            ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
+                            bd = tc::make_sdesc(b0 + k * 32, 16, 1024);
+                        }
+                        tc::mma_bf16(d, ad, bd, idesc, (kc | k) != 0);
+                    }
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == kStages) { stage = 0; ph ^= 1; }
                 }
-                tc::mma_bf16(tmem, ad, bd, idesc, (kc | k) != 0);
+                if (!ok) break;
+                tc::mma_commit(&acc_full[buf]);
             }
-            tc::mma_commit(&empty[stage]);
         }
-        tc::mma_commit(done);
-    }
-
-    if (warp < 4) {
+    } else {
         // ---------------- epilogue: TMEM -> fp32 partials
-        const bool ok = tc::mbar_wait(done, 0, abrt, a.status);
-        tc::tc_fence_after();
-        const int row = tile * kBM + warp * 32 + lane;
-        float* out = a.part + (((long long)split * a.batch + b) * out_rows + row) * a.rp + rc * 256;
-        for (int c0 = 0; c0 < nN; c0 += 32) {
-            uint32_t v[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            tc::tmem_ld_wait();
-            if (ok && row < out_rows) {
-                const int nv = min(32, nN - c0);
-                for (int j = 0; j < nv; j += 4)
-                    *reinterpret_cast<float4*>(out + c0 + j) =
-                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                                    __uint_as_float(v[j + 3]));
+        const int q = warp & 3;                        // TMEM lane quarter of this warp
+        int it = 0;
+        for (int u = blockIdx.x; u < units && !*abrt; u += gridDim.x, ++it) {
+            int b, split, tile, kc0, nk;
+            unit_of(u, b, split, tile, kc0, nk);
+            const int buf = it & 1;
+            if (!tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abrt, a.status)) break;
+            tc::tc_fence_after();
+            const int row = tile * kBM + q * 32 + lane;
+            float* out = a.part + (((long long)split * a.batch + b) * out_rows + row) * a.rp;
+            for (int c0 = 0; c0 < nN; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256 + c0), v);
+                tc::tmem_ld_wait();
+                if (row < out_rows) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(out + c0 + j) =
+                            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                        __uint_as_float(v[j + 3]));
+                }
             }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
         }
-        tc::tc_fence_before();
     }
     __syncthreads();
-    if (warp == kPassWarps - 1) {
+    if (warp == kMmaWarp) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -600,10 +647,11 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
 
 // Qt[b][j][k] = bf16(Q[b][k][j]) for j < r; zero rows r <= j < rp.
 __global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp, long long ldqt, const float* Q,
-                                                           bf16* Qt)
+                                                           bf16* Qt, int* counter)
 {
     __shared__ float tile[32][33];
     const int b = blockIdx.z, k0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) counter[b] = 0;   // for dion_rsum
     for (int kk = threadIdx.y; kk < 32; kk += 8) {
         const int k = k0 + kk, j = j0 + threadIdx.x;
         tile[kk][threadIdx.x] = (k < n && j < r) ? Q[((long long)b * n + k) * r + j] : 0.f;
@@ -615,9 +663,6 @@ __global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp,
     }
 }
 
-// R = sum of the split partials (fp32, pitch rp), R16 = bf16(R) (columns r..rp-1
-// zero), and per-chunk column sums of squares normpart[b][chunk][c] over rows
-// chunk*kRChunk ..: every sum in a fixed order, so results are reproducible.
 // ------------------------------------------------- wide ranks (rp > 256)
 // B = M + G as bf16 once, row-major (B16, pitch pb) and transposed (B16T,
 // pitch mp), for the two TMA GEMMs that replace the fused passes when the
@@ -711,10 +756,19 @@ __global__ void __launch_bounds__(256) dion_transpose16_kernel(int rows, int col
 
 constexpr int kRChunk = 32;
 
+// R = sum of the split partials (fp32, pitch rp), R16 = bf16(R) (columns r..rp-1
+// zero), and per-chunk column sums of squares normpart[b][chunk][c] over rows
+// chunk*kRChunk ..: every sum in a fixed order, so results are reproducible.
+// The CTA that finishes last for matrix b (a per-matrix arrival counter,
+// zeroed by dion_prep_qt_kernel earlier in the step) reduces the chunks in
+// order into inv[b][c] = 1 / max(||R_c||, floor) (0 for padding columns) and
+// resets the counter.
 __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, int splits, int batch,
                                                         const float* __restrict__ part, float* __restrict__ R,
-                                                        bf16* __restrict__ R16, float* __restrict__ normpart)
+                                                        bf16* __restrict__ R16, float* __restrict__ normpart,
+                                                        int* counter, float* inv, float floor_nrm, int* status)
 {
+    __shared__ int s_last;
     const int b = blockIdx.y, chunk = blockIdx.x, nchunks = gridDim.x;
     const int j0 = chunk * kRChunk, j1 = min(n, j0 + kRChunk);
     const long long pstride = (long long)batch * n * rp;
@@ -732,17 +786,15 @@ __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, in
         }
         normpart[((long long)b * nchunks + chunk) * rp + c] = ss;
     }
-}
-
-// inv[b][c] = 1 / max(||R_c||, floor) for c < r, 0 for the padding columns.
-__global__ void __launch_bounds__(256) dion_norm_final_kernel(int r, int rp, int nchunks,
-                                                              const float* __restrict__ normpart, float* inv,
-                                                              float floor_nrm, int* status)
-{
-    const int b = blockIdx.x;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&counter[b], 1) == nchunks - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
     for (int c = threadIdx.x; c < rp; c += blockDim.x) {
         float t = 0.f;
-        for (int k = 0; k < nchunks; ++k) t += normpart[((long long)b * nchunks + k) * rp + c];
+        for (int k = 0; k < nchunks; ++k) t += __ldcg(&normpart[((long long)b * nchunks + k) * rp + c]);
         float v = 0.f;
         if (c < r) {
             v = 1.f / fmaxf(sqrtf(t), floor_nrm);
@@ -750,59 +802,32 @@ __global__ void __launch_bounds__(256) dion_norm_final_kernel(int r, int rp, int
         }
         inv[(long long)b * rp + c] = v;
     }
+    if (threadIdx.x == 0) counter[b] = 0;
 }
 
-// Q = R * inv (the caller's n x r float32 state) and Q16 = bf16(Q) (n x rp operand).
-__global__ void __launch_bounds__(256) dion_qemit_kernel(int n, int r, int rp, long long total,
+// Q = R * inv (the caller's n x r float32 state) and Q16 = bf16(Q) (n x rp
+// operand), four columns per thread.
+__global__ void __launch_bounds__(256) dion_qemit_kernel(int n, int r, int rp, int rows,
                                                          const float* __restrict__ R, const float* __restrict__ inv,
                                                          float* __restrict__ Q, bf16* __restrict__ Q16)
 {
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int c = (int)(e % rp);
-        const long long row = e / rp;                 // b * n + j
-        const int b = (int)(row / n);
-        const float q = R[e] * inv[(long long)b * rp + c];
-        Q16[e] = __float2bfloat16_rn(q);
-        if (c < r) Q[row * r + c] = q;
+    const int upr = rp >> 2;
+    const int total = rows * upr;                     // rows = batch * n
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int row = e / upr, c = (e - row * upr) * 4, b = row / n;
+        const float4 x = *reinterpret_cast<const float4*>(R + (size_t)row * rp + c);
+        const float4 s = *reinterpret_cast<const float4*>(inv + (size_t)b * rp + c);
+        const float q[4] = {x.x * s.x, x.y * s.y, x.z * s.z, x.w * s.w};
+        *reinterpret_cast<uint2*>(Q16 + (size_t)row * rp + c) =
+            make_uint2(tc::pack_bf16x2(q[0], q[1]), tc::pack_bf16x2(q[2], q[3]));
+        float* qo = Q + (size_t)row * r + c;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (c + t < r) qo[t] = q[t];
     }
 }
 
 }  // namespace
-
-// Q_j <- R_j / max(||R_j||, floor) over the n rows of R (pitch ldr >= r).
-__global__ void __launch_bounds__(256) dion_colnorm_tc_kernel(int n, int r, long long ldr, const float* R, float* Q,
-                                                              float* inv_out, float floor_nrm, int* status)
-{
-    __shared__ float red[8][33];
-    __shared__ float s_inv[32];
-    const int b = blockIdx.y, tx = threadIdx.x, ty = threadIdx.y;
-    const int j = blockIdx.x * 32 + tx;
-    const float* Rb = R + (size_t)b * n * ldr;
-    float s = 0.f;
-    if (j < r)
-        for (int i = ty; i < n; i += 8) {
-            const float v = Rb[(size_t)i * ldr + j];
-            s = fmaf(v, v, s);
-        }
-    red[ty][tx] = s;
-    __syncthreads();
-    if (ty == 0) {
-        float t = 0.f;
-        for (int k = 0; k < 8; ++k) t += red[k][tx];
-        const float inv = 1.f / fmaxf(sqrtf(t), floor_nrm);
-        s_inv[tx] = inv;
-        if (j < r) {
-            inv_out[(size_t)b * r + j] = inv;
-            if (!isfinite(t)) atomicOr(status, kStatusNonFinite);
-        }
-    }
-    __syncthreads();
-    if (j < r) {
-        float* Qb = Q + (size_t)b * n * r;
-        for (int i = ty; i < n; i += 8) Qb[(size_t)i * r + j] = Rb[(size_t)i * ldr + j] * s_inv[tx];
-    }
-}
 
 static unsigned grid_for(long long work, int per = 256 * 4)
 {
@@ -813,9 +838,11 @@ static unsigned grid_for(long long work, int per = 256 * 4)
 }
 
 template <bool MN_A>
-static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm, dim3 grid, const PassArgs& pa,
-                               cudaStream_t st)
+static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm, const PassArgs& pa, cudaStream_t st)
 {
+    const int out_rows = MN_A ? pa.n : pa.m;
+    const long long units = cdiv(out_rows, kBM) * (long long)pa.splits * pa.batch;
+    const dim3 grid((unsigned)std::min<long long>(units, num_sms()));
     static bool attr[2] = {false, false};
     auto k = vec ? dion_pass_kernel<MN_A, true> : dion_pass_kernel<MN_A, false>;
     if (!attr[vec]) {
@@ -845,13 +872,14 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     float* normp = (float*)(ws + L.normp);
     const long long np = (long long)align_up((size_t)n, 8);
     const bool vec = (n % 8) == 0;
-    const int rchunks = (int)cdiv(rp, 256);
     const int nbox = rp < 256 ? rp : 256;
 
     DION_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
     // 1. Qt = bf16(Q^T)
+    int* rcount = (int*)(ws + L.rcount);
+    const float floor_nrm = 1e-12f * sqrtf((float)n);
     DION_TRY(launch("dion_prep_qt", dion_prep_qt_kernel, dim3((unsigned)cdiv(n, 32), (unsigned)cdiv(rp, 32), batch),
-                    dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16));
+                    dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16, rcount));
     const long long mp = (long long)align_up((size_t)m, 8);
     if (L.wide) {
         // 2'. B = M + G once in bf16 (and B^T); P = B Q as a TMA GEMM into part (one split)
@@ -884,7 +912,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         DION_TRY(tc_gemm<256>("dion_btp_tc", tA2, tB2, m, e2, st));
         const int nchunks = (int)cdiv(n, kRChunk);
         DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
-                        batch, (const float*)part, R, R16, normp));
+                        batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
     } else {
     // 2. P partials = B Q
     CUtensorMap tmQt;
@@ -893,9 +921,8 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int kchunks = (int)cdiv(n, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
-        DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, dim3((unsigned)cdiv(m, kBM), splits * rchunks, batch),
-                                    pa, st));
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status};
+        DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, pa, st));
         // 3-5. CholeskyQR2; its first pass reads the split partials of P directly, its
         // last product writes P (float32, P0) and P16 = bf16(P)
         DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st));
@@ -908,22 +935,18 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int kchunks = (int)cdiv(m, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit_r);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, rchunks, kcps, kchunks, M, G, part, status};
-        DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, dim3((unsigned)cdiv(n, kBM), splits * rchunks, batch),
-                                   pa, st));
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status};
+        DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, pa, st));
         // 7. R = sum of partials, R16, column norms, Q = R / ||R_j||, Q16
         const int nchunks = (int)cdiv(n, kRChunk);
         DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp,
-                        splits, batch, (const float*)part, R, R16, normp));
+                        splits, batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
     }
     }
     {
-        const int nchunks = (int)cdiv(n, kRChunk);
-        DION_TRY(launch("dion_norm_final", dion_norm_final_kernel, dim3(batch), dim3(256), 0, st, r, rp, nchunks,
-                        (const float*)normp, inv, 1e-12f * sqrtf((float)n), status));
-        const long long total = (long long)batch * n * rp;
-        DION_TRY(launch("dion_qemit", dion_qemit_kernel, dim3(grid_for(total)), dim3(256), 0, st, n, r, rp, total,
-                        (const float*)R, (const float*)inv, Q, Q16));
+        const int rows = batch * n;
+        DION_TRY(launch("dion_qemit", dion_qemit_kernel, dim3(grid_for((long long)rows * (rp / 4))), dim3(256), 0, st,
+                        n, r, rp, rows, (const float*)R, (const float*)inv, Q, Q16));
     }
     // 9. M and X updates
     CUtensorMap tmPa, tmR, tmQ;

@@ -14,6 +14,7 @@ struct DionLayout {
     size_t status, P0, P1, R, S, W, dead, inv, Ppart, Qt16, P16, R16, Q16;
     size_t P3, P3b, Z3, S6; // CholeskyQR2 operands of the tensor-core path (P3, P3b: bf16 terms of the panel)
     size_t normp;           // per-chunk column sums of squares of R
+    size_t rcount;          // per matrix arrival counter of the column-norm reduction
     size_t emax;            // per matrix max|S - I| of the second CholeskyQR Gram
     int nbc;                // block size of the blocked Cholesky (0: one CTA per matrix)
     size_t ZJ, A3;          // its diagonal-block inverse and panel terms

@@ -45,9 +45,8 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int r, int rp, con
     const int b = blockIdx.y;
     const size_t pn = (size_t)m * rp;
     const int upr = rp >> 2;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total4;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int i = (int)(e / upr), c = (int)(e - (long long)i * upr) * 4;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < (int)total4; e += gridDim.x * blockDim.x) {
+        const int i = e / upr, c = (e - i * upr) * 4;
         const size_t o = (size_t)b * pn + (size_t)i * rp + c;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < r) {
@@ -98,15 +97,16 @@ __global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, c
     const float* Sb = S6 + (size_t)b * nparts * rr;
     bf16* z0 = Z3 + (size_t)3 * b * zs;
     float em = 0.f;
-    const long long total = (long long)r * ldz;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int i = (int)(e / ldz), k = (int)(e % ldz);
+    const int total = r * ldz;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int i = e / ldz, k = e - i * ldz;
         float v = 0.f;
         if (k <= i) {
             const size_t o = (size_t)i * r + k;
-            float sv = Sb[o];
-            for (int q = 1; q < nparts; ++q) sv += Sb[q * rr + o];
+            float sv = 0.f;
+#pragma unroll
+            for (int q = 0; q < 6; ++q)
+                if (q < nparts) sv += Sb[q * rr + o];
             const float ev = sv - (i == k ? 1.f : 0.f);
             em = fmaxf(em, isfinite(ev) ? fabsf(ev) : 1e30f);
             v = (k < i) ? -sv : 1.f - 0.5f * ev;
@@ -201,10 +201,9 @@ __global__ void __launch_bounds__(256) qr_panel_split_kernel(int r, int rows, in
     const float* Sb = S + (size_t)b * r * r;
     const size_t ts = (size_t)r * nb;
     bf16* a0 = A3 + (size_t)3 * b * ts;
-    const long long total = (long long)rows * nb;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int i = (int)(e / nb), c = (int)(e % nb);
+    const int total = rows * nb;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int i = e / nb, c = e - i * nb;
         const float v = c < w ? Sb[(size_t)i * r + c] : 0.f;
         bf16 h1, h2, h3;
         split3(v, h1, h2, h3);
