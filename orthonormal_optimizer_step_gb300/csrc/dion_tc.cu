@@ -126,6 +126,7 @@ constexpr size_t kPassSmem = (size_t)kStages * kStage + 1024 + 256;
 // tile; tiles fastest, so concurrent CTAs share the operand chunks in L2).
 // MN_A = false: P = B Q, A tile = 128 rows of B x 64 columns, K-major.
 // MN_A = true:  R = B^T P, A tile = 64 rows of B x 128 columns, MN-major.
+// The other operand (Q16 or P16, row-major K x rp) is MN-major in both.
 // Producer warps form B = M + G in registers (two chunks of loads in flight,
 // across unit boundaries), round to bf16 and write the swizzled A tile; one
 // thread adds the operand tile (Q^T or P) by TMA.  The accumulator is double
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
     const int tiles = (out_rows + kBM - 1) / kBM;
     const int units = tiles * a.splits * a.batch;
     const int nN = a.rp;                               // MMA N (multiple of 64, at most 256)
-    const uint32_t b_bytes = MN_A ? (uint32_t)(nN / 64) * 8192u : (uint32_t)nN * 128u;
+    const uint32_t b_bytes = (uint32_t)(nN / 64) * 8192u;   // B operand: nN/64 MN-major 64 x 64 boxes
     auto unit_of = [&](int u, int& b, int& split, int& tile, int& kc0, int& nk) {
         tile = u % tiles;
         split = (u / tiles) % a.splits;
@@ -227,12 +228,8 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
             const int k0 = (kc0 + kc) * kBK;
             if (threadIdx.x == 0) {
                 tc::mbar_arrive_expect_tx(&full[stage], b_bytes);
-                if (MN_A) {
-                    for (int blk = 0; blk * 64 < nN; ++blk)
-                        tc::tma_load_3d(sA + kAB + blk * 8192, &tmB, &full[stage], blk * 64, k0, b);
-                } else {
-                    tc::tma_load_3d(sA + kAB, &tmB, &full[stage], k0, 0, b);
-                }
+                for (int blk = 0; blk * 64 < nN; ++blk)
+                    tc::tma_load_3d(sA + kAB + blk * 8192, &tmB, &full[stage], blk * 64, k0, b);
             }
 #pragma unroll
             for (int v = 0; v < kPerProducer; ++v) *reinterpret_cast<uint4*>(sA + off[v]) = sum_pack8(cur[v]);
@@ -248,7 +245,7 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, MN_A);
+            const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, true);
             int stage = 0, it = 0;
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < units && !*abrt; u += gridDim.x, ++it) {
@@ -265,14 +262,9 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
                     const uint32_t a0 = tc::smem_u32(smem + stage * kStage), b0 = a0 + kAB;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        uint64_t ad, bd;
-                        if (MN_A) {
-                            ad = tc::make_sdesc(a0 + k * 2048, 8192, 1024);
-                            bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
-                        } else {
-                            ad = tc::make_sdesc(a0 + k * 32, 16, 1024);
-                            bd = tc::make_sdesc(b0 + k * 32, 16, 1024);
-                        }
+                        const uint64_t ad = MN_A ? tc::make_sdesc(a0 + k * 2048, 8192, 1024)
+                                                 : tc::make_sdesc(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
                         tc::mma_bf16(d, ad, bd, idesc, (kc | k) != 0);
                     }
                     tc::mma_commit(&empty[stage]);
@@ -754,6 +746,26 @@ __global__ void __launch_bounds__(256) dion_transpose16_kernel(int rows, int col
     }
 }
 
+// Q16 = bf16(Q) (n x rp, row-major, padding columns zero): the MN-major
+// operand of B Q (rp <= 256).  Four columns per thread.  Also zeroes the
+// column-norm arrival counters of dion_rsum for this step.
+__global__ void __launch_bounds__(256) dion_prep_q16_kernel(int n, int r, int rp, const float* __restrict__ Q,
+                                                            bf16* __restrict__ Q16, int* counter)
+{
+    const int b = blockIdx.y, upr = rp >> 2, total = n * upr;
+    if (blockIdx.x == 0 && threadIdx.x == 0) counter[b] = 0;
+    const float* Qb = Q + (size_t)b * n * r;
+    bf16* Ob = Q16 + (size_t)b * n * rp;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int j = e / upr, c = (e - j * upr) * 4;
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = (c + t < r) ? Qb[(size_t)j * r + c + t] : 0.f;
+        *reinterpret_cast<uint2*>(Ob + (size_t)j * rp + c) =
+            make_uint2(tc::pack_bf16x2(v[0], v[1]), tc::pack_bf16x2(v[2], v[3]));
+    }
+}
+
 constexpr int kRChunk = 32;
 
 // R = sum of the split partials (fp32, pitch rp), R16 = bf16(R) (columns r..rp-1
@@ -872,14 +884,19 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     float* normp = (float*)(ws + L.normp);
     const long long np = (long long)align_up((size_t)n, 8);
     const bool vec = (n % 8) == 0;
-    const int nbox = rp < 256 ? rp : 256;
 
     DION_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
     // 1. Qt = bf16(Q^T)
     int* rcount = (int*)(ws + L.rcount);
     const float floor_nrm = 1e-12f * sqrtf((float)n);
-    DION_TRY(launch("dion_prep_qt", dion_prep_qt_kernel, dim3((unsigned)cdiv(n, 32), (unsigned)cdiv(rp, 32), batch),
-                    dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16, rcount));
+    if (L.wide) {   // 1. Qt = bf16(Q^T), the K-major operand of the B Q GEMM
+        DION_TRY(launch("dion_prep_qt", dion_prep_qt_kernel, dim3((unsigned)cdiv(n, 32), (unsigned)cdiv(rp, 32), batch),
+                        dim3(32, 8), 0, st, n, r, rp, np, (const float*)Q, Qt16, rcount));
+    } else {        // 1. Q16 = bf16(Q), the MN-major operand of the fused pass
+        DION_TRY(launch("dion_prep_qt", dion_prep_q16_kernel,
+                        dim3((unsigned)std::min<long long>(cdiv((long long)n * (rp / 4), 256), 1024), batch), dim3(256),
+                        0, st, n, r, rp, (const float*)Q, Q16, rcount));
+    }
     const long long mp = (long long)align_up((size_t)m, 8);
     if (L.wide) {
         // 2'. B = M + G once in bf16 (and B^T); P = B Q as a TMA GEMM into part (one split)
@@ -916,7 +933,8 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     } else {
     // 2. P partials = B Q
     CUtensorMap tmQt;
-    if (!make_tmap_3d(&tmQt, Qt16, TmapType::BF16, n, rp, batch, np * 2, rp * np * 2, 64, nbox)) return DION_ERR_CUDA;
+    if (!make_tmap_3d(&tmQt, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 64))
+        return DION_ERR_CUDA;
     {
         const int kchunks = (int)cdiv(n, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit);
