@@ -805,8 +805,16 @@ __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, in
     if (!s_last) return;
     __threadfence();
     for (int c = threadIdx.x; c < rp; c += blockDim.x) {
-        float t = 0.f;
-        for (int k = 0; k < nchunks; ++k) t += __ldcg(&normpart[((long long)b * nchunks + k) * rp + c]);
+        // eight interleaved partial sums (loads in flight), combined in a fixed order
+        const float* np_ = normpart + (long long)b * nchunks * rp + c;
+        float t8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int k = 0;
+        for (; k + 8 <= nchunks; k += 8) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) t8[q] += __ldcg(np_ + (long long)(k + q) * rp);
+        }
+        for (; k < nchunks; ++k) t8[k & 7] += __ldcg(np_ + (long long)k * rp);
+        const float t = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
         float v = 0.f;
         if (c < r) {
             v = 1.f / fmaxf(sqrtf(t), floor_nrm);
@@ -988,11 +996,11 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         if (ua.kchunks <= 4) {
             static bool pattr = false;
             if (!pattr) {
-                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<2, 2>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<2, 2>()));
+                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<3, 2>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<3, 2>()));
                 pattr = true;
             }
-            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<2, 2>, dim3(grid), dim3(192), upd_smem<2, 2>(),
+            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<3, 2>, dim3(grid), dim3(192), upd_smem<3, 2>(),
                             st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
         } else {
             static bool pattr_w = false;
