@@ -781,22 +781,57 @@ __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, in
                                                         int* counter, float* inv, float floor_nrm, int* status)
 {
     __shared__ int s_last;
+    __shared__ float4 s_ss[4][64];
     const int b = blockIdx.y, chunk = blockIdx.x, nchunks = gridDim.x;
-    const int j0 = chunk * kRChunk, j1 = min(n, j0 + kRChunk);
+    const int j0 = chunk * kRChunk;
     const long long pstride = (long long)batch * n * rp;
-    for (int c = threadIdx.x; c < rp; c += blockDim.x) {
-        float ss = 0.f;
-#pragma unroll 4
-        for (int j = j0; j < j1; ++j) {
-            const long long o = ((long long)b * n + j) * rp + c;
-            float v = part[o];
-            for (int q = 1; q < splits; ++q) v += part[o + q * pstride];
-            if (c >= r) v = 0.f;
-            R[o] = v;
-            R16[o] = __float2bfloat16_rn(v);
-            ss = fmaf(v, v, ss);
+    // thread = 4 columns (cg) x rows j0 + rl, j0 + rl + 4, ... (8 rows): float4
+    // accesses; 256 columns per pass over the rp columns
+    const int cg = threadIdx.x & 63, rl = threadIdx.x >> 6;
+    for (int cb = 0; cb < rp; cb += 256) {
+    const int c = cb + cg * 4;
+    float4 ss = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < rp) {
+        float4 v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int j = j0 + rl + 4 * t;
+            v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < n) {
+                const long long o = ((long long)b * n + j) * rp + c;
+                v[t] = *reinterpret_cast<const float4*>(part + o);
+                for (int q = 1; q < splits; ++q) {
+                    const float4 u = *reinterpret_cast<const float4*>(part + o + q * pstride);
+                    v[t].x += u.x; v[t].y += u.y; v[t].z += u.z; v[t].w += u.w;
+                }
+            }
         }
-        normpart[((long long)b * nchunks + chunk) * rp + c] = ss;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int j = j0 + rl + 4 * t;
+            if (j < n) {
+                float4 x = v[t];
+                if (c >= r) x.x = 0.f;
+                if (c + 1 >= r) x.y = 0.f;
+                if (c + 2 >= r) x.z = 0.f;
+                if (c + 3 >= r) x.w = 0.f;
+                const long long o = ((long long)b * n + j) * rp + c;
+                *reinterpret_cast<float4*>(R + o) = x;
+                *reinterpret_cast<uint2*>(R16 + o) = make_uint2(tc::pack_bf16x2(x.x, x.y), tc::pack_bf16x2(x.z, x.w));
+                ss.x = fmaf(x.x, x.x, ss.x); ss.y = fmaf(x.y, x.y, ss.y);
+                ss.z = fmaf(x.z, x.z, ss.z); ss.w = fmaf(x.w, x.w, ss.w);
+            }
+        }
+    }
+    s_ss[rl][cg] = ss;
+    __syncthreads();
+    if (rl == 0 && c < rp) {   // the four row lanes, in a fixed order
+        const float4 a0 = s_ss[0][cg], a1 = s_ss[1][cg], a2 = s_ss[2][cg], a3 = s_ss[3][cg];
+        *reinterpret_cast<float4*>(normpart + ((long long)b * nchunks + chunk) * rp + c) =
+            make_float4((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y), (a0.z + a1.z) + (a2.z + a3.z),
+                        (a0.w + a1.w) + (a2.w + a3.w));
+    }
+    __syncthreads();
     }
     __threadfence();
     __syncthreads();
