@@ -95,6 +95,30 @@ dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt,
                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * dion_step_batched with mu, lr and weight_decay read on the device, when the
+ * step's kernels run, from hyper[0], hyper[1], hyper[2] (three float32 values
+ * in device memory, 4-byte aligned, owned by the caller).  The step enqueues
+ * only kernels and asynchronous memsets on cuda_stream, allocates nothing and
+ * never synchronizes, so it can be captured in a CUDA graph once and replayed
+ * every step while the caller writes the schedule's values into hyper (with
+ * any stream-ordered copy) between replays; the same shapes, pointers and
+ * workspace are used by every replay.  The first call for a shape should be
+ * made outside a capture (it sets per-kernel launch attributes once).
+ * Both entry points form 1 - mu, 1 - lr*weight_decay and lr*sqrt(m/n) on the
+ * device with the same operations, so equal values give identical results.
+ * Non-finite values in hyper set the non-finite bit of the status word (see
+ * dion_get_status); the step still runs.  Argument errors (as for
+ * dion_step_batched, plus hyper == NULL or misaligned) return
+ * DION_ERR_INVALID_ARG before any launch.
+ * This serves a live learning-rate schedule under graph replay (the pages'
+ * optimizer takes the learning rate and decay as per-step scalars).
+ */
+dion_status dion_step_batched_dev(int batch, int m, int n, int r, dion_dtype dt,
+                                  void* X, const void* G, float* M, float* Q,
+                                  const float* hyper,
+                                  void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Upper bound, in bytes, of the fixed device scratch of
  * dion_step_batched_static (64 MiB).  Every GPU that loads libdion holds an
  * array of this size until the process exits.

@@ -24,7 +24,8 @@ DION_OK, DION_ERR_INVALID_ARG, DION_ERR_UNSUPPORTED, DION_ERR_WORKSPACE, DION_ER
 DION_F32, DION_BF16 = 0, 1
 
 # The exported symbols of include/dion.h.
-EXPORTS = ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
+EXPORTS = ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_dev",
+           "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
            "dion_get_status", "dion_status_string", "dion_profile_begin", "dion_profile_end",
            "dion_profile_count", "dion_profile_entry", "dion_profile_dropped")
 
@@ -56,6 +57,7 @@ def lib() -> ctypes.CDLL:
                                                           ctypes.POINTER(c_size), ctypes.POINTER(c_int)]
         L.dion_step_batched.argtypes = ([c_int] * 5 + [vp, vp, vp, vp] + [c_float] * 3 + [vp, c_size, vp])
         L.dion_step_batched_static.argtypes = ([c_int] * 5 + [vp, vp, vp, vp] + [c_float] * 3 + [vp])
+        L.dion_step_batched_dev.argtypes = ([c_int] * 5 + [vp, vp, vp, vp, vp] + [vp, c_size, vp])
         L.muon_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]
         L.muon_ns_batched.argtypes = ([c_int] * 5 + [vp, vp, vp, vp, c_int, ctypes.POINTER(c_float)]
                                       + [c_float] * 3 + [vp, c_size, vp])
@@ -68,7 +70,8 @@ def lib() -> ctypes.CDLL:
         L.dion_profile_dropped.argtypes = []
         L.dion_profile_entry.argtypes = [c_int, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_int),
                                          ctypes.POINTER(ctypes.c_double)]
-        for f in ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
+        for f in ("dion_workspace_size", "dion_workspace_panels", "dion_step_batched", "dion_step_batched_dev",
+                  "dion_step_batched_static", "muon_workspace_size", "muon_ns_batched",
                   "dion_get_status", "dion_profile_begin", "dion_profile_end", "dion_profile_count",
                   "dion_profile_entry", "dion_profile_dropped"):
             getattr(L, f).restype = c_int
@@ -149,12 +152,15 @@ def new_workspace(nbytes: int, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def dion_step_batched(X, G, M, Q, *, mu: float, lr: float, weight_decay: float = 0.0, workspace=None,
-                      stream=None):
+def dion_step_batched(X, G, M, Q, *, mu: float = None, lr: float = None, weight_decay: float = 0.0, hyper=None,
+                      workspace=None, stream=None):
     """One Dion step on a megabatch: X, G [batch, m, n] (fp32 or bf16), M
     [batch, m, n] fp32 and Q [batch, n, r] fp32 are CUDA tensors; X, M and Q
     are updated in place.  Returns the workspace used (it holds the status
-    word, see dion_get_status)."""
+    word, see dion_get_status).  With `hyper` (a float32 CUDA tensor holding
+    mu, lr, weight_decay) the scalars are read on the device when the step
+    runs (dion_step_batched_dev), so a CUDA graph of the call follows new
+    values written into `hyper`; mu, lr and weight_decay are then ignored."""
     batch, m, n = _shape3(X)
     r = Q.shape[-1]
     dt = _dtype_code(X)
@@ -163,6 +169,15 @@ def dion_step_batched(X, G, M, Q, *, mu: float, lr: float, weight_decay: float =
             raise ValueError("tensors must be contiguous")
     if workspace is None:
         workspace = new_workspace(dion_workspace_size(batch, m, n, r, dt), X.device)
+    if hyper is not None:
+        if hyper.dtype.itemsize != 4 or hyper.numel() < 3 or not hyper.is_contiguous() or not hyper.is_cuda:
+            raise ValueError("hyper must be a contiguous float32 CUDA tensor of (mu, lr, weight_decay)")
+        code = lib().dion_step_batched_dev(batch, m, n, r, dt, _ptr(X), _ptr(G), _ptr(M), _ptr(Q), _ptr(hyper),
+                                           _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+        _check(code, "dion_step_batched_dev")
+        return workspace
+    if mu is None or lr is None:
+        raise ValueError("mu and lr are required unless hyper is given")
     code = lib().dion_step_batched(batch, m, n, r, dt, _ptr(X), _ptr(G), _ptr(M), _ptr(Q), float(mu), float(lr),
                                    float(weight_decay), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(code, "dion_step_batched")

@@ -171,9 +171,9 @@ extern "C" dion_status dion_workspace_panels(int batch, int m, int n, int r, dio
     return DION_OK;
 }
 
-extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G,
-                                         float* M, float* Q, float mu, float lr, float weight_decay,
-                                         void* workspace, size_t workspace_bytes, void* cuda_stream)
+static dion_status dion_step_any(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
+                                 float* Q, float mu, float lr, float weight_decay, const float* hyper, void* workspace,
+                                 size_t workspace_bytes, void* cuda_stream)
 {
     if (!dion_shape_ok(batch, m, n, r, dt)) return DION_ERR_INVALID_ARG;
     if (!X || !G || !M || !Q) return DION_ERR_INVALID_ARG;
@@ -184,8 +184,25 @@ extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dt
     if (L.tc && (long long)batch * n * (L.rp / 4) >= (1ll << 31)) return DION_ERR_UNSUPPORTED;
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return DION_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    if (L.tc) return dion_step_tc(batch, m, n, r, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);
-    return dion_step_simt(batch, m, n, r, dt, X, G, M, Q, mu, lr, weight_decay, (char*)workspace, L, st);
+    if (L.tc) return dion_step_tc(batch, m, n, r, X, G, M, Q, mu, lr, weight_decay, hyper, (char*)workspace, L, st);
+    return dion_step_simt(batch, m, n, r, dt, X, G, M, Q, mu, lr, weight_decay, hyper, (char*)workspace, L, st);
+}
+
+extern "C" dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G,
+                                         float* M, float* Q, float mu, float lr, float weight_decay,
+                                         void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    return dion_step_any(batch, m, n, r, dt, X, G, M, Q, mu, lr, weight_decay, nullptr, workspace, workspace_bytes,
+                         cuda_stream);
+}
+
+extern "C" dion_status dion_step_batched_dev(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G,
+                                             float* M, float* Q, const float* hyper, void* workspace,
+                                             size_t workspace_bytes, void* cuda_stream)
+{
+    if (!hyper || ((uintptr_t)hyper & 3u)) return DION_ERR_INVALID_ARG;
+    return dion_step_any(batch, m, n, r, dt, X, G, M, Q, 0.f, 0.f, 0.f, hyper, workspace, workspace_bytes,
+                         cuda_stream);
 }
 
 static bool muon_shape_ok(int batch, int m, int n, int head_dim, dion_dtype dt)

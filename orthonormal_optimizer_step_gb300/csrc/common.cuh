@@ -21,6 +21,32 @@ enum : int { kStatusPivot = 1, kStatusNonFinite = 2 };
 // (error O(E^2), below float32 rounding).
 constexpr float kNearIdentityTol = 1e-4f;
 
+// mu, lr and weight decay of a Dion step: given by value, or read on the device
+// from hyper[0..2] when hyper is set, so that a captured CUDA graph of the
+// step follows whatever the caller writes there between replays.  The derived
+// factors 1 - mu, 1 - lr wd and lr sqrt(m/n) are formed on the device in both
+// cases, each operation rounded once, so the two forms give the same bits.
+struct StepHyper {
+    float mu, lr, wd, sqrt_mn;
+    const float* hyper;
+    __device__ __forceinline__ void get(float& one_minus_mu, float& decay, float& scale) const
+    {
+        float mu_ = mu, lr_ = lr, wd_ = wd;
+        if (hyper) {
+            mu_ = hyper[0];
+            lr_ = hyper[1];
+            wd_ = hyper[2];
+        }
+        one_minus_mu = __fsub_rn(1.f, mu_);
+        decay = __fsub_rn(1.f, __fmul_rn(lr_, wd_));
+        scale = __fmul_rn(lr_, sqrt_mn);
+    }
+    __device__ __forceinline__ bool finite() const
+    {
+        return !hyper || (isfinite(hyper[0]) && isfinite(hyper[1]) && isfinite(hyper[2]));
+    }
+};
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v);

@@ -316,7 +316,7 @@ struct UpdArgs {
     float* M;
     const bf16* G;
     bf16* X;
-    float one_minus_mu, decay, scale;
+    StepHyper hp;
     int* status;
 };
 
@@ -338,6 +338,10 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
     int* abort_flag = (int*)(tmem_slot + 1);
     volatile int* abrt = abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float one_minus_mu, decay, scale;
+    a.hp.get(one_minus_mu, decay, scale);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && !a.hp.finite())
+        atomicOr(a.status, kStatusNonFinite);
     const int nt = blockIdx.x, mt = blockIdx.y, b = blockIdx.z;
 
     if (threadIdx.x == 0) {
@@ -416,8 +420,8 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
                     float xv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        mv[e] = mv[e] + __bfloat162float(gh[e]) - a.one_minus_mu * __uint_as_float(pr[8 * q + e]);
-                        xv[e] = a.decay * __bfloat162float(xh[e]) - a.scale * __uint_as_float(pq[8 * q + e]);
+                        mv[e] = mv[e] + __bfloat162float(gh[e]) - one_minus_mu * __uint_as_float(pr[8 * q + e]);
+                        xv[e] = decay * __bfloat162float(xh[e]) - scale * __uint_as_float(pq[8 * q + e]);
                     }
                     *reinterpret_cast<float4*>(a.M + o + 8 * q) = make_float4(mv[0], mv[1], mv[2], mv[3]);
                     *reinterpret_cast<float4*>(a.M + o + 8 * q + 4) = make_float4(mv[4], mv[5], mv[6], mv[7]);
@@ -426,9 +430,9 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
             } else {
                 const int nv = min(32, a.n - j0);
                 for (int e = 0; e < nv; ++e) {
-                    a.M[o + e] = a.M[o + e] + __bfloat162float(a.G[o + e]) - a.one_minus_mu * __uint_as_float(pr[e]);
-                    a.X[o + e] = __float2bfloat16_rn(a.decay * __bfloat162float(a.X[o + e]) -
-                                                     a.scale * __uint_as_float(pq[e]));
+                    a.M[o + e] = a.M[o + e] + __bfloat162float(a.G[o + e]) - one_minus_mu * __uint_as_float(pr[e]);
+                    a.X[o + e] = __float2bfloat16_rn(decay * __bfloat162float(a.X[o + e]) -
+                                                     scale * __uint_as_float(pq[e]));
                 }
             }
         }
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
 //   warp 4: TMA producer     warp 5: MMA issuer     warps 0..3: epilogue
 struct UpdPArgs {
     int m, n, batch, kchunks, tiles_m, tiles_n;
-    float one_minus_mu, decay, scale;
+    StepHyper hp;
     int* status;
 };
 
@@ -483,6 +487,10 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
     int* abort_flag = (int*)(tmem_slot + 1);
     volatile int* abrt = abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float one_minus_mu, decay, scale;
+    a.hp.get(one_minus_mu, decay, scale);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && !a.hp.finite())
+        atomicOr(a.status, kStatusNonFinite);
     const int per_mat = a.tiles_m * a.tiles_n, tiles = a.batch * per_mat;
 
     if (threadIdx.x == 0) {
@@ -592,10 +600,10 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                     const uint32_t gchunk = h * 4 + (c >> 1);
                     const bf16* gh = reinterpret_cast<const bf16*>(e + kEM + tc::sw128_offset(row, gchunk)) + (c & 1) * 4;
                     float4 mv = *pm;
-                    mv.x = mv.x + __bfloat162float(gh[0]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 0]);
-                    mv.y = mv.y + __bfloat162float(gh[1]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 1]);
-                    mv.z = mv.z + __bfloat162float(gh[2]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 2]);
-                    mv.w = mv.w + __bfloat162float(gh[3]) - a.one_minus_mu * __uint_as_float(pr[4 * c + 3]);
+                    mv.x = mv.x + __bfloat162float(gh[0]) - one_minus_mu * __uint_as_float(pr[4 * c + 0]);
+                    mv.y = mv.y + __bfloat162float(gh[1]) - one_minus_mu * __uint_as_float(pr[4 * c + 1]);
+                    mv.z = mv.z + __bfloat162float(gh[2]) - one_minus_mu * __uint_as_float(pr[4 * c + 2]);
+                    mv.w = mv.w + __bfloat162float(gh[3]) - one_minus_mu * __uint_as_float(pr[4 * c + 3]);
                     *pm = mv;
                 }
 #pragma unroll
@@ -606,7 +614,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                     float o[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        o[q] = a.decay * __bfloat162float(xh[q]) - a.scale * __uint_as_float(pq[8 * c + q]);
+                        o[q] = decay * __bfloat162float(xh[q]) - scale * __uint_as_float(pq[8 * c + q]);
                     *px = pack8(o);
                 }
             }
@@ -909,8 +917,9 @@ static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm
 }
 
 dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* Gv, float* M, float* Q, float mu,
-                         float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st)
+                         float lr, float wd, const float* hyper, char* ws, const DionLayout& L, cudaStream_t st)
 {
+    const StepHyper hp{mu, lr, wd, sqrtf((float)m / (float)n), hyper};
     bf16* X = (bf16*)Xv;
     const bf16* G = (const bf16*)Gv;
     const int rp = L.rp;
@@ -1026,8 +1035,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int tm = (int)cdiv(m, kBM), tn = (int)cdiv(n, kUBN);
         const long long tiles = (long long)tm * tn * batch;
         const int grid = (int)std::min<long long>(tiles, num_sms());
-        UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n),
-                    status};
+        UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, hp, status};
         if (ua.kchunks <= 4) {
             static bool pattr = false;
             if (!pattr) {
@@ -1054,8 +1062,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
             DION_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUpdSmem));
             attr[vec] = true;
         }
-        UpdArgs ua{m, n, rp, (int)cdiv(rp, kBK), M, G, X, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n),
-                   status};
+        UpdArgs ua{m, n, rp, (int)cdiv(rp, kBK), M, G, X, hp, status};
         DION_TRY(launch("dion_update_tc", k, dim3((unsigned)cdiv(n, kUBN), (unsigned)cdiv(m, kBM), batch), dim3(192),
                         kUpdSmem, st, tmPa, tmR, tmQ, ua));
     }

@@ -64,10 +64,10 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                             bf16* P16, char* ws, const struct DionLayout& L, int* status, cudaStream_t st);
 
 dion_status dion_step_simt(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
-                           float* Q, float mu, float lr, float wd, char* ws, const DionLayout& L,
+                           float* Q, float mu, float lr, float wd, const float* hyper, char* ws, const DionLayout& L,
                            cudaStream_t st);
 dion_status dion_step_tc(int batch, int m, int n, int r, void* X, const void* G, float* M, float* Q, float mu,
-                         float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st);
+                         float lr, float wd, const float* hyper, char* ws, const DionLayout& L, cudaStream_t st);
 dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void* G, float* M, void* O, int steps,
                     const float* coeff, float mu, float lr, float wd, char* ws, const MuonLayout& L,
                     cudaStream_t st);

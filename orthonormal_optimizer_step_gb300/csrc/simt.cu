@@ -53,17 +53,26 @@ __global__ void __launch_bounds__(256) colnorm_kernel(int n, int r, long long ld
 template <typename T>
 struct EpDionUpdate {
     T* X; const T* G; float* M; long long sb; long long ld;
-    float one_minus_mu, decay, scale;
+    StepHyper hp;
     __device__ __forceinline__ void operator()(int b, int i, int j, float prt, float pqt) const {
+        float one_minus_mu, decay, scale;
+        hp.get(one_minus_mu, decay, scale);
         const long long o = b * sb + i * ld + j;
         M[o] = M[o] + to_f(G[o]) - one_minus_mu * prt;
         X[o] = from_f<T>(decay * to_f(X[o]) - scale * pqt);
     }
 };
 
+// Non-finite device-side hyperparameters set the status word.
+__global__ void hyper_check_kernel(const float* hyper, int* status)
+{
+    if (threadIdx.x == 0 && !(isfinite(hyper[0]) && isfinite(hyper[1]) && isfinite(hyper[2])))
+        atomicOr(status, kStatusNonFinite);
+}
+
 template <typename T>
 static dion_status dion_simt_t(int batch, int m, int n, int r, T* X, const T* G, float* M, float* Q, float mu,
-                               float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st)
+                               float lr, float wd, const float* hyper, char* ws, const DionLayout& L, cudaStream_t st)
 {
     int* status = (int*)(ws + L.status);
     float* P0 = (float*)(ws + L.P0);
@@ -88,18 +97,20 @@ static dion_status dion_simt_t(int batch, int m, int n, int r, T* X, const T* G,
     DION_TRY(launch("dion_colnorm", colnorm_kernel, dim3((unsigned)cdiv(r, 32), batch), dim3(32, 8), 0, st, n, r,
                     (long long)r, (const float*)R, Q, inv, 1e-12f * sqrtf((float)n), status));
     // M, X updates
-    EpDionUpdate<T> ep{X, G, M, mn, n, 1.f - mu, 1.f - lr * wd, lr * sqrtf((float)m / (float)n)};
+    EpDionUpdate<T> ep{X, G, M, mn, n, StepHyper{mu, lr, wd, sqrtf((float)m / (float)n), hyper}};
+    if (hyper) DION_TRY(launch("dion_hyper_check", hyper_check_kernel, dim3(1), dim3(32), 0, st, hyper, status));
     DION_TRY((gemm_simt<2>("dion_update_simt", batch, m, n, r, LdA<float, true>{P0, mr, r},
                            LdB<float, false>{R, nr, r}, LdB<float, false>{Q, nr, r}, ep, st)));
     return DION_OK;
 }
 
 dion_status dion_step_simt(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
-                           float* Q, float mu, float lr, float wd, char* ws, const DionLayout& L, cudaStream_t st)
+                           float* Q, float mu, float lr, float wd, const float* hyper, char* ws, const DionLayout& L,
+                           cudaStream_t st)
 {
     if (dt == DION_F32)
-        return dion_simt_t<float>(batch, m, n, r, (float*)X, (const float*)G, M, Q, mu, lr, wd, ws, L, st);
-    return dion_simt_t<bf16>(batch, m, n, r, (bf16*)X, (const bf16*)G, M, Q, mu, lr, wd, ws, L, st);
+        return dion_simt_t<float>(batch, m, n, r, (float*)X, (const float*)G, M, Q, mu, lr, wd, hyper, ws, L, st);
+    return dion_simt_t<bf16>(batch, m, n, r, (bf16*)X, (const bf16*)G, M, Q, mu, lr, wd, hyper, ws, L, st);
 }
 
 // ---------------------------------------------------------- Newton-Schulz ----

@@ -85,6 +85,15 @@ def test_step_rejects_bad_arguments_before_launch(lib):
         == od.DION_ERR_WORKSPACE
     assert lib.dion_step_batched(1, 64, 64, 8, 0, fake, fake, fake, fake, 0.9, 0.01, 0.0,
                                  ctypes.c_void_p((1 << 24) + 16), big, None) == od.DION_ERR_WORKSPACE
+    # device-scalar variant: missing or misaligned hyper, and the shape checks of dion_step_batched
+    assert lib.dion_step_batched_dev(1, 64, 64, 8, 0, fake, fake, fake, fake, None, ws, big, None) \
+        == od.DION_ERR_INVALID_ARG
+    assert lib.dion_step_batched_dev(1, 64, 64, 8, 0, fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 2), ws, big,
+                                     None) == od.DION_ERR_INVALID_ARG
+    assert lib.dion_step_batched_dev(1, 64, 32, 33, 0, fake, fake, fake, fake, fake, ws, big, None) \
+        == od.DION_ERR_INVALID_ARG
+    assert lib.dion_step_batched_dev(1, 64, 64, 8, 0, fake, fake, fake, fake, fake, ws, 16, None) \
+        == od.DION_ERR_WORKSPACE
     coeff = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
     # Muon: neither X nor O
     assert lib.muon_ns_batched(1, 64, 64, 0, 1, None, fake, None, None, 5, coeff, 0.9, 0.01, 0.0, ws, big, None) \

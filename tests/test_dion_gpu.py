@@ -179,3 +179,53 @@ def test_blocked_factorization_reads_no_stale_workspace():
     for a, b in zip(*outs):
         assert torch.isfinite(a.float()).all()
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_device_scalars_follow_schedule_under_graph_replay(dtype):
+    """dion_step_batched_dev captured once in a CUDA graph and replayed while
+    the caller writes a new (mu, lr, weight_decay) into device memory gives the
+    same bits as direct calls with those values passed by value."""
+    g = wl.Group(2, 192, 320)
+    r = 48
+    X, M, Q = wl.make_state(g, r, dtype, DEV, seed=41)
+    grads = [wl.make_grad(g, 1.0, dtype, DEV, 41, s) for s in range(4)]
+    schedule = [(0.9, 0.02, 0.01), (0.9, 0.01, 0.01), (0.8, 0.005, 0.0), (0.95, 0.03, 0.1)]
+    ref = [t.clone() for t in (X, M, Q)]
+    ws_ref = od.new_workspace(od.dion_workspace_size(2, 192, 320, r, od.DION_BF16 if dtype == torch.bfloat16
+                                                     else od.DION_F32), DEV)
+    for (mu, lr, wd), Gs in zip(schedule, grads):
+        od.dion_step_batched(ref[0], Gs, ref[1], ref[2], mu=mu, lr=lr, weight_decay=wd, workspace=ws_ref)
+    # graph: static input buffer for G, device scalars
+    Gbuf = grads[0].clone()
+    hyper = torch.tensor(schedule[0], dtype=torch.float32, device=DEV)
+    ws = od.new_workspace(ws_ref.numel(), DEV)
+    cur = [t.clone() for t in (X, M, Q)]
+    warm = [t.clone() for t in (X, M, Q)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # first call outside the capture (launch attributes)
+        od.dion_step_batched(warm[0], Gbuf, warm[1], warm[2], hyper=hyper, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        od.dion_step_batched(cur[0], Gbuf, cur[1], cur[2], hyper=hyper, workspace=ws)
+    for (mu, lr, wd), Gs in zip(schedule, grads):
+        Gbuf.copy_(Gs)
+        hyper.copy_(torch.tensor([mu, lr, wd], dtype=torch.float32))
+        graph.replay()
+    torch.cuda.synchronize()
+    assert od.dion_get_status(ws) == 0
+    for a, b in zip(cur, ref):
+        assert torch.equal(a, b)
+
+
+def test_device_scalars_non_finite_sets_status():
+    g = wl.Group(1, 64, 96)
+    X, M, Q = wl.make_state(g, 8, torch.bfloat16, DEV, seed=43)
+    G = wl.make_grad(g, 1.0, torch.bfloat16, DEV, 43, 0)
+    hyper = torch.tensor([0.9, float("nan"), 0.0], dtype=torch.float32, device=DEV)
+    ws = od.dion_step_batched(X, G, M, Q, hyper=hyper)
+    torch.cuda.synchronize()
+    assert od.dion_get_status(ws) & 2
