@@ -318,18 +318,26 @@ def run_gb300(args, rank, world, local_rank):
         msteps = max(1, args.steps // 2)
         for _ in range(max(1, args.warmup)):
             muon_step()
-        mms = timed(muon_step, msteps) / msteps
+        mms_streams = timed(muon_step, msteps) / msteps
         saved_streams = list(streams)
         streams[:] = [main for _ in state]
+        # Each Newton-Schulz GEMM fills the GPU by itself, so at large shapes the
+        # groups run faster one after another (concurrent GEMMs on huge matrices
+        # evict each other's tiles from L2); both launch orders are timed and the
+        # faster one is reported, with which it was.
+        mms_seq = timed(muon_step, msteps) / msteps
         mprof = od.profile(max_launches=64 * msteps * len(state) * (w.ns_steps + 2) + 64)
-        mms_seq = timed(muon_step, msteps, mprof) / msteps
+        timed(muon_step, msteps, mprof)
         streams[:] = saved_streams
+        mms = min(mms_streams, mms_seq)
         mk = mprof.read()
         nfl = sum(ns_flops(st["g"], w.ns_steps) for st in state)
         gemm_ms = sum(v[1] for k, v in mk.items() if k.startswith("ns_") and ("gram" in k or "poly" in k
                                                                               or "axpy" in k))
         ach = nfl / (gemm_ms / msteps * 1e-3) / 1e12 if gemm_ms > 0 else None
-        muon = {"ms_per_step": mms, "ms_per_step_one_stream": mms_seq, "tflops_step": nfl / (mms * 1e-3) / 1e12,
+        muon = {"ms_per_step": mms, "group_streams": bool(mms_streams <= mms_seq),
+                "ms_per_step_streams": mms_streams, "ms_per_step_one_stream": mms_seq,
+                "tflops_step": nfl / (mms * 1e-3) / 1e12,
                 "roofline": {"bound": "tensor", "kernel": "ns gemm chain", "achieved": ach,
                              "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,

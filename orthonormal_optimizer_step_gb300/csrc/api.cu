@@ -109,8 +109,7 @@ MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt)
         const size_t h = sizeof(uint16_t);
         L.Xa = carve(off, nb * L.s * L.lp * h);
         L.Xb = carve(off, nb * L.s * L.lp * h);
-        L.XTa = carve(off, nb * L.l * L.sp * h);
-        L.XTb = carve(off, nb * L.l * L.sp * h);
+        L.XTa = L.XTb = off;   // no transposed copy: Bm Y reads Y MN-major
         L.A = carve(off, nb * L.s * L.sp * h);
         L.Bm = carve(off, nb * L.s * L.sp * h);
     } else {

@@ -28,7 +28,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
 struct MuonLayout {
     int heads, hd, s, l, nb;   // blocks per matrix, block width, Gram side, long side, total blocks
     bool tr, tc;               // blocks transposed (m > hd); tensor-core path
-    int lp, sp;                // row pitches (elements) of the bf16 s x l and l x s / s x s buffers
+    int lp, sp;                // row pitches (elements) of the bf16 s x l and s x s buffers
     size_t status, nrm, Xa, Xb, XTa, XTb, A, Bm, total;
 };
 MuonLayout muon_layout(int batch, int m, int n, int head_dim, dion_dtype dt);

@@ -7,10 +7,10 @@
 //   Y <- Y / (||Y||_F + 1e-7)
 //   repeat: A = Y Y^T ; Bm = b A + c A A ; Y <- a Y + Bm Y
 // The three products are the persistent tcgen05 GEMM of tc_gemm.cuh.  Y is
-// kept in bf16 in both layouts (Y: s x l and Y^T: l x s) so that every product
-// reads K-major operands: A = Y Y^T contracts over l (rows of Y), and
-// Bm Y = Bm (Y^T)^T contracts over s (rows of Y^T).  The last product writes
-// both layouts from its epilogue.
+// kept in bf16 as s x l only: A = Y Y^T and Bm = b A + c A A read K-major
+// operands, and Bm Y reads both operands MN-major (Y row-major with K = s
+// rows, and Bm, which is symmetric, as its own transpose), so no transposed
+// copy of Y is ever written.
 #include "internal.h"
 #include "ns_common.cuh"
 #include "tc_gemm.cuh"
@@ -31,14 +31,13 @@ int num_sms()
     return n;
 }
 
-// Scaled bf16 copies of each block in both layouts.  Source block bh = (b, h):
-// y(i, c) = M or G at row i, column h*hd + c.  With tr (m > hd) the block is
-// transposed: Y[p][q] = y(q, p).  Writes Y (s x lp pitch) and YT (l x sp).
+// Scaled bf16 copy of each block as s x l (pitch ldy).  Source block bh =
+// (b, h): y(i, c) = M or G at row i, column h*hd + c.  With tr (m > hd) the
+// block is transposed: Y[p][q] = y(q, p), written through the shared tile.
 template <typename T>
 __global__ void __launch_bounds__(256) ns_load_tc_kernel(int m, int n, int hd, int heads, int tr, const T* G,
                                                          const float* M, const float* nrm, float eps, bf16* Y,
-                                                         long long ldy, long long sy, bf16* YT, long long ldyt,
-                                                         long long syt)
+                                                         long long ldy, long long sy)
 {
     __shared__ float tile[32][33];
     const int bh = blockIdx.z, b = bh / heads, h = bh % heads;
@@ -55,18 +54,17 @@ __global__ void __launch_bounds__(256) ns_load_tc_kernel(int m, int n, int hd, i
         tile[ii][threadIdx.x] = v;
     }
     __syncthreads();
-    // same orientation as the source: row i, column c
-    bf16* same = tr ? YT + bh * syt : Y + bh * sy;
-    const long long lds = tr ? ldyt : ldy;
-    bf16* other = tr ? Y + bh * sy : YT + bh * syt;
-    const long long ldo = tr ? ldy : ldyt;
-    for (int ii = threadIdx.y; ii < 32; ii += 8) {
-        const int i = i0 + ii, c = c0 + threadIdx.x;
-        if (i < m && c < hd) same[(long long)i * lds + c] = __float2bfloat16_rn(tile[ii][threadIdx.x]);
-    }
-    for (int cc = threadIdx.y; cc < 32; cc += 8) {
-        const int c = c0 + cc, i = i0 + threadIdx.x;
-        if (i < m && c < hd) other[(long long)c * ldo + i] = __float2bfloat16_rn(tile[threadIdx.x][cc]);
+    bf16* Yb = Y + bh * sy;
+    if (!tr) {
+        for (int ii = threadIdx.y; ii < 32; ii += 8) {
+            const int i = i0 + ii, c = c0 + threadIdx.x;
+            if (i < m && c < hd) Yb[(long long)i * ldy + c] = __float2bfloat16_rn(tile[ii][threadIdx.x]);
+        }
+    } else {
+        for (int cc = threadIdx.y; cc < 32; cc += 8) {
+            const int c = c0 + cc, i = i0 + threadIdx.x;
+            if (i < m && c < hd) Yb[(long long)c * ldy + i] = __float2bfloat16_rn(tile[threadIdx.x][cc]);
+        }
     }
 }
 
@@ -92,7 +90,43 @@ __global__ void __launch_bounds__(256) ns_finish_tc_kernel(int batch, int m, int
     }
 }
 
+// ns_finish_tc_kernel for transposed blocks (m > hd): Y[bh] is hd x m, so
+// O(i, c) = Y[c][i]; 32 x 32 tiles through shared memory keep both sides
+// coalesced.
+template <typename T>
+__global__ void __launch_bounds__(256) ns_finish_tr_kernel(int m, int n, int hd, int heads, const bf16* Y,
+                                                           long long ldy, long long sy, T* O, T* X, float decay,
+                                                           float scale)
+{
+    __shared__ float tile[32][33];
+    const int bh = blockIdx.z, b = bh / heads, h = bh % heads;
+    const int i0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    const bf16* Yb = Y + bh * sy;
+    for (int cc = threadIdx.y; cc < 32; cc += 8) {
+        const int c = c0 + cc, i = i0 + threadIdx.x;
+        tile[cc][threadIdx.x] = (c < hd && i < m) ? __bfloat162float(Yb[(long long)c * ldy + i]) : 0.f;
+    }
+    __syncthreads();
+    for (int ii = threadIdx.y; ii < 32; ii += 8) {
+        const int i = i0 + ii, c = c0 + threadIdx.x;
+        if (i < m && c < hd) {
+            const long long e = ((long long)b * m + i) * n + (long long)h * hd + c;
+            const float o = tile[threadIdx.x][ii];
+            if (O) O[e] = from_f<T>(o);
+            if (X) X[e] = from_f<T>(decay * to_f(X[e]) - scale * o);
+        }
+    }
+}
+
 static int pick_bn(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+
+static cudaError_t gemm_bn_mn(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K,
+                              const TcGemmEpi& ep, cudaStream_t st)
+{
+    if (bn == 64) return tc_gemm<64, true>(name, ta, tb, K, ep, st);
+    if (bn == 128) return tc_gemm<128, true>(name, ta, tb, K, ep, st);
+    return tc_gemm<256, true>(name, ta, tb, K, ep, st);
+}
 
 static cudaError_t gemm_bn(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K,
                            const TcGemmEpi& ep, cudaStream_t st)
@@ -110,13 +144,11 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
     float* nrm = (float*)(ws + L.nrm);
     bf16* Ya = (bf16*)(ws + L.Xa);
     bf16* Yb = (bf16*)(ws + L.Xb);
-    bf16* YTa = (bf16*)(ws + L.XTa);
-    bf16* YTb = (bf16*)(ws + L.XTb);
     bf16* A = (bf16*)(ws + L.A);
     bf16* Bm = (bf16*)(ws + L.Bm);
     const int s = L.s, l = L.l, nb = L.nb;
     const long long lp = L.lp, sp = L.sp;
-    const long long sy = (long long)s * lp, syt = (long long)l * sp, sa = (long long)s * sp;
+    const long long sy = (long long)s * lp, sa = (long long)s * sp;
 
     DION_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
     DION_TRY(cudaMemsetAsync(nrm, 0, sizeof(float) * nb, st));
@@ -130,23 +162,21 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
     dim3 lgrid((unsigned)cdiv(L.hd, 32), (unsigned)cdiv(m, 32), (unsigned)nb);
     if (dt == DION_F32)
         DION_TRY(launch("ns_load_tc", ns_load_tc_kernel<float>, lgrid, dim3(32, 8), 0, st, m, n, L.hd, L.heads,
-                        (int)L.tr, (const float*)G, (const float*)M, (const float*)nrm, 1e-7f, Ya, lp, sy, YTa, sp,
-                        syt));
+                        (int)L.tr, (const float*)G, (const float*)M, (const float*)nrm, 1e-7f, Ya, lp, sy));
     else
         DION_TRY(launch("ns_load_tc", ns_load_tc_kernel<bf16>, lgrid, dim3(32, 8), 0, st, m, n, L.hd, L.heads,
-                        (int)L.tr, (const bf16*)G, (const float*)M, (const float*)nrm, 1e-7f, Ya, lp, sy, YTa, sp,
-                        syt));
+                        (int)L.tr, (const bf16*)G, (const float*)M, (const float*)nrm, 1e-7f, Ya, lp, sy));
 
     const int bn_s = pick_bn(s), bn_l = pick_bn(l);
     const int tm = (int)cdiv(s, 128);
     for (int k = 0; k < steps; ++k) {
-        CUtensorMap tYa_a, tYa_b, tA_a, tA_b, tBm_a, tYTa_b;
+        CUtensorMap tYa_a, tYa_b, tA_a, tA_b, tBm_mn, tYa_mn;
         bool ok = make_tmap_3d(&tYa_a, Ya, TmapType::BF16, l, s, nb, lp * 2, sy * 2, 64, 128) &&
                   make_tmap_3d(&tYa_b, Ya, TmapType::BF16, l, s, nb, lp * 2, sy * 2, 64, bn_s) &&
                   make_tmap_3d(&tA_a, A, TmapType::BF16, s, s, nb, sp * 2, sa * 2, 64, 128) &&
                   make_tmap_3d(&tA_b, A, TmapType::BF16, s, s, nb, sp * 2, sa * 2, 64, bn_s) &&
-                  make_tmap_3d(&tBm_a, Bm, TmapType::BF16, s, s, nb, sp * 2, sa * 2, 64, 128) &&
-                  make_tmap_3d(&tYTa_b, YTa, TmapType::BF16, s, l, nb, sp * 2, syt * 2, 64, bn_l);
+                  make_tmap_3d(&tBm_mn, Bm, TmapType::BF16, s, s, nb, sp * 2, sa * 2, 64, 64) &&
+                  make_tmap_3d(&tYa_mn, Ya, TmapType::BF16, l, s, nb, lp * 2, sy * 2, 64, 64);
         if (!ok) return DION_ERR_CUDA;
         // A = Y Y^T
         TcGemmEpi e1{s, s, tm, (int)cdiv(s, bn_s), nb, A, sp, sa, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, nullptr, 1, 1, 0, 0u, 0u};
@@ -155,23 +185,31 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
         TcGemmEpi e2{s, s, tm, (int)cdiv(s, bn_s), nb, Bm, sp, sa, A, sp, sa, nullptr, 0, 0, coeff[1], coeff[2],
                      status, nullptr, 1, 1, 0, 0u, 0u};
         DION_TRY(gemm_bn(bn_s, "ns_poly_tc", tA_a, tA_b, s, e2, st));
-        // Y' = a Y + Bm Y, written as Y' and Y'^T
-        TcGemmEpi e3{s, l, tm, (int)cdiv(l, bn_l), nb, Yb, lp, sy, Ya, lp, sy, YTb, sp, syt, coeff[0], 1.f, status, nullptr, 1, 1, 0, 0u, 0u};
-        DION_TRY(gemm_bn(bn_l, "ns_axpy_tc", tBm_a, tYTa_b, s, e3, st));
+        // Y' = a Y + Bm Y: both operands MN-major (Bm symmetric, Y row-major with K = s rows)
+        TcGemmEpi e3{s, l, tm, (int)cdiv(l, bn_l), nb, Yb, lp, sy, Ya, lp, sy, nullptr, 0, 0, coeff[0], 1.f, status,
+                     nullptr, 1, 1, 0, 0u, 0u};
+        DION_TRY(gemm_bn_mn(bn_l, "ns_axpy_tc", tBm_mn, tYa_mn, s, e3, st));
         std::swap(Ya, Yb);
-        std::swap(YTa, YTb);
     }
-    const bf16* src = L.tr ? YTa : Ya;
-    const long long lds = L.tr ? sp : lp, sbs = L.tr ? syt : sy;
+    const float decay = 1.f - lr * wd, scale = lr * sqrtf((float)m / (float)n);
+    if (L.tr) {
+        const dim3 fgrid((unsigned)cdiv(m, 32), (unsigned)cdiv(L.hd, 32), (unsigned)nb);
+        if (dt == DION_F32)
+            DION_TRY(launch("ns_finish_tc", ns_finish_tr_kernel<float>, fgrid, dim3(32, 8), 0, st, m, n, L.hd,
+                            L.heads, (const bf16*)Ya, lp, sy, (float*)O, (float*)X, decay, scale));
+        else
+            DION_TRY(launch("ns_finish_tc", ns_finish_tr_kernel<bf16>, fgrid, dim3(32, 8), 0, st, m, n, L.hd,
+                            L.heads, (const bf16*)Ya, lp, sy, (bf16*)O, (bf16*)X, decay, scale));
+        return DION_OK;
+    }
     const long long total = (long long)batch * m * n;
     const unsigned fchunks = (unsigned)std::min<long long>(cdiv(total, 256 * 4), 65535);
-    const float decay = 1.f - lr * wd, scale = lr * sqrtf((float)m / (float)n);
     if (dt == DION_F32)
         DION_TRY(launch("ns_finish_tc", ns_finish_tc_kernel<float>, dim3(fchunks), dim3(256), 0, st, batch, m, n, L.hd,
-                        L.heads, src, lds, sbs, (float*)O, (float*)X, decay, scale));
+                        L.heads, (const bf16*)Ya, lp, sy, (float*)O, (float*)X, decay, scale));
     else
         DION_TRY(launch("ns_finish_tc", ns_finish_tc_kernel<bf16>, dim3(fchunks), dim3(256), 0, st, batch, m, n,
-                        L.hd, L.heads, src, lds, sbs, (bf16*)O, (bf16*)X, decay, scale));
+                        L.hd, L.heads, (const bf16*)Ya, lp, sy, (bf16*)O, (bf16*)X, decay, scale));
     return DION_OK;
 }
 
