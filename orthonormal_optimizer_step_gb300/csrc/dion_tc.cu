@@ -1024,7 +1024,30 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         !make_tmap_3d(&tmR, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN) ||
         !make_tmap_3d(&tmQ, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN))
         return DION_ERR_CUDA;
-    if (vec) {
+    if (vec && L.wide) {
+        // wide ranks: the two products as persistent 128 x 256 TMA GEMMs with
+        // the updates fused into their epilogues (M and X in place):
+        //   M <- M + G - (1 - mu) P R^T,   X <- (1 - lr wd) X - lr sqrt(m/n) P Q^T
+        CUtensorMap tP, tRb, tQb;
+        if (!make_tmap_3d(&tP, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||
+            !make_tmap_3d(&tRb, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256) ||
+            !make_tmap_3d(&tQb, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256))
+            return DION_ERR_CUDA;
+        const long long mn = (long long)m * n;
+        TcGemmEpi e1{};
+        e1.M = m; e1.N = n; e1.tiles_m = (int)cdiv(m, kBM); e1.tiles_n = (int)cdiv(n, 256); e1.batch = batch;
+        e1.Cf = M; e1.ldc = n; e1.sc = mn;
+        e1.auxf = M; e1.ldauxf = n; e1.sauxf = mn; e1.alpha = 1.f;
+        e1.aux2 = G; e1.ldaux2 = n; e1.saux2 = mn; e1.alpha2 = 1.f;
+        e1.hp = hp; e1.hp_mode = 1; e1.status = status; e1.nseg = 1; e1.zmul = 1;
+        DION_TRY(tc_gemm<256>("dion_update_tc", tP, tRb, rp, e1, st));
+        TcGemmEpi e2{};
+        e2.M = m; e2.N = n; e2.tiles_m = e1.tiles_m; e2.tiles_n = e1.tiles_n; e2.batch = batch;
+        e2.C = X; e2.ldc = n; e2.sc = mn;
+        e2.aux = X; e2.ldaux = n; e2.saux = mn;
+        e2.hp = hp; e2.hp_mode = 2; e2.status = status; e2.nseg = 1; e2.zmul = 1;
+        DION_TRY(tc_gemm<256>("dion_update_tc", tP, tQb, rp, e2, st));
+    } else if (vec) {
         // persistent TMA-epilogue pass (needs 16-byte aligned rows of M, G, X)
         CUtensorMap tmM, tmG, tmX;
         const long long mn = (long long)m * n;

@@ -45,6 +45,13 @@ struct TcGemmEpi {
     // `lower`, only tiles holding an element on or below the diagonal
     const int* gate;
     int lower;
+    // second addend (bf16), added after the float32 one: C += alpha2 * aux2
+    const bf16* aux2; long long ldaux2, saux2; float alpha2;
+    // hp_mode != 0: the step scalars come from hp (see StepHyper), formed in
+    // the epilogue: 1 -> beta = -(1 - mu); 2 -> alpha = 1 - lr wd,
+    // beta = -lr sqrt(m/n).  Non-finite device values set the status word.
+    StepHyper hp;
+    int hp_mode;
 };
 
 template <int BN>
@@ -74,11 +81,12 @@ __device__ __forceinline__ bool tc_tile_on(const TcGemmEpi& ep, int b, int tm, i
     return true;
 }
 
-__device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row, int col0, const uint32_t (&v)[32])
+__device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row, int col0, const uint32_t (&v)[32],
+                                             float alpha, float beta)
 {
     float acc[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = ep.beta * __uint_as_float(v[i]);
+    for (int i = 0; i < 32; ++i) acc[i] = beta * __uint_as_float(v[i]);
     const int ncol = min(32, ep.N - col0);
     if (ep.auxf) {
         const float* ap = ep.auxf + b * ep.sauxf + (long long)row * ep.ldauxf + col0;
@@ -86,13 +94,15 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 u = *reinterpret_cast<const float4*>(ap + j);
-                acc[j] = fmaf(ep.alpha, u.x, acc[j]);
-                acc[j + 1] = fmaf(ep.alpha, u.y, acc[j + 1]);
-                acc[j + 2] = fmaf(ep.alpha, u.z, acc[j + 2]);
-                acc[j + 3] = fmaf(ep.alpha, u.w, acc[j + 3]);
+                acc[j] = fmaf(alpha, u.x, acc[j]);
+                acc[j + 1] = fmaf(alpha, u.y, acc[j + 1]);
+                acc[j + 2] = fmaf(alpha, u.z, acc[j + 2]);
+                acc[j + 3] = fmaf(alpha, u.w, acc[j + 3]);
             }
         } else {
-            for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, ap[i], acc[i]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncol) acc[i] = fmaf(alpha, ap[i], acc[i]);
         }
     } else if (ep.aux) {
         const bf16* ap = ep.aux + b * ep.saux + (long long)row * ep.ldaux + col0;
@@ -102,10 +112,29 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
                 uint4 u = *reinterpret_cast<const uint4*>(ap + 8 * j);
                 const bf16* h = reinterpret_cast<const bf16*>(&u);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[8 * j + e] = fmaf(ep.alpha, __bfloat162float(h[e]), acc[8 * j + e]);
+                for (int e = 0; e < 8; ++e) acc[8 * j + e] = fmaf(alpha, __bfloat162float(h[e]), acc[8 * j + e]);
             }
         } else {
-            for (int i = 0; i < ncol; ++i) acc[i] = fmaf(ep.alpha, __bfloat162float(ap[i]), acc[i]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncol) acc[i] = fmaf(alpha, __bfloat162float(ap[i]), acc[i]);
+        }
+    }
+    if (ep.aux2) {
+        const bf16* ap = ep.aux2 + b * ep.saux2 + (long long)row * ep.ldaux2 + col0;
+        if (ncol == 32 && ((uintptr_t)ap & 15u) == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 u = *reinterpret_cast<const uint4*>(ap + 8 * j);
+                const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[8 * j + e] = fmaf(ep.alpha2, __bfloat162float(h[e]), acc[8 * j + e]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncol) acc[i] = fmaf(ep.alpha2, __bfloat162float(ap[i]), acc[i]);
         }
     }
     if (ep.Cs3) {
@@ -137,7 +166,9 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
                 *reinterpret_cast<uint4*>(sp + 2 * ep.scs3 + j) = make_uint4(t3[0], t3[1], t3[2], t3[3]);
             }
         } else {
-            for (int i = 0; i < ncol; ++i) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (i >= ncol) break;
                 const bf16 h1 = __float2bfloat16_rn(acc[i]);
                 const float r1 = acc[i] - __bfloat162float(h1);
                 const bf16 h2 = __float2bfloat16_rn(r1);
@@ -154,7 +185,9 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(fp + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
         } else {
-            for (int i = 0; i < ncol; ++i) fp[i] = acc[i];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncol) fp[i] = acc[i];
         }
         if (!ep.C) return;             // else also a bf16 copy with the same pitches
     }
@@ -171,11 +204,15 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
             *reinterpret_cast<uint4*>(cp + 8 * j) = u;
         }
     } else {
-        for (int i = 0; i < ncol; ++i) cp[i] = __float2bfloat16_rn(acc[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncol) cp[i] = __float2bfloat16_rn(acc[i]);
     }
     if (ep.CT) {
         bf16* tp = ep.CT + b * ep.sct + (long long)col0 * ep.ldct + row;
-        for (int i = 0; i < ncol; ++i) tp[(long long)i * ep.ldct] = __float2bfloat16_rn(acc[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncol) tp[(long long)i * ep.ldct] = __float2bfloat16_rn(acc[i]);
     }
 }
 
@@ -302,6 +339,18 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         const int q = warp & 3;          // TMEM lane quarter this warp may access
+        float alpha = ep.alpha, beta = ep.beta;
+        if (ep.hp_mode) {
+            float one_minus_mu, decay, scale;
+            ep.hp.get(one_minus_mu, decay, scale);
+            if (ep.hp_mode == 1) {
+                beta = -one_minus_mu;
+            } else {
+                alpha = decay;
+                beta = -scale;
+            }
+            if (blockIdx.x == 0 && warp == 2 && lane == 0 && !ep.hp.finite()) atomicOr(ep.status, kStatusNonFinite);
+        }
         int it = 0;
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
             const int b = t / per_mat, rem = t % per_mat;
@@ -319,7 +368,7 @@ __global__ void __launch_bounds__(192, 1)
                 tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
                 tc::tmem_ld_wait();
                 const int col0 = tn * BN + c0;
-                if (row < ep.M && col0 < ep.N) tc_epi_store(ep, b, row, col0, v);
+                if (row < ep.M && col0 < ep.N) tc_epi_store(ep, b, row, col0, v, alpha, beta);
             }
             tc::tc_fence_before();
             __syncwarp();
