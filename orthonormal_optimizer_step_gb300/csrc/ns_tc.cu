@@ -90,6 +90,34 @@ __global__ void __launch_bounds__(256) ns_finish_tc_kernel(int batch, int m, int
     }
 }
 
+// ns_finish_tc_kernel with eight columns per thread (n % 8 == 0, hd % 8 == 0).
+template <typename T>
+__global__ void __launch_bounds__(256) ns_finish_vec_kernel(int batch, int m, int n, int hd, int heads,
+                                                            const bf16* src, long long lds, long long sbs, T* O, T* X,
+                                                            float decay, float scale)
+{
+    const int upr = n >> 3;
+    const long long total = (long long)batch * m * upr;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long row = e / upr;                 // b * m + i
+        const int col = (int)(e - row * upr) * 8;
+        const int b = (int)(row / m), i = (int)(row - (long long)b * m);
+        const int h = col / hd, c = col - h * hd;
+        float o[8];
+        ld8(src + ((long long)b * heads + h) * sbs + (long long)i * lds + c, o);
+        const long long eo = row * n + col;
+        if (O) st8(O + eo, o);
+        if (X) {
+            float x[8];
+            ld8(X + eo, x);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x[t] = decay * x[t] - scale * o[t];
+            st8(X + eo, x);
+        }
+    }
+}
+
 // ns_finish_tc_kernel for transposed blocks (m > hd): Y[bh] is hd x m, so
 // O(i, c) = Y[c][i]; 32 x 32 tiles through shared memory keep both sides
 // coalesced.
@@ -153,7 +181,16 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
     DION_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
     DION_TRY(cudaMemsetAsync(nrm, 0, sizeof(float) * nb, st));
     const unsigned chunks = (unsigned)std::min<long long>(cdiv((long long)m * L.hd, 256 * 8), 64);
-    if (dt == DION_F32)
+    const bool vec8 = (L.hd % 8) == 0 && (n % 8) == 0;
+    if (vec8) {
+        const unsigned vchunks = (unsigned)std::min<long long>(cdiv((long long)m * (L.hd / 8), 256 * 4), 64);
+        if (dt == DION_F32)
+            DION_TRY(launch("ns_prep", ns_prep_vec_kernel<float>, dim3(vchunks, nb), dim3(256), 0, st, m, n, L.hd,
+                            L.heads, (const float*)G, M, mu, nrm));
+        else
+            DION_TRY(launch("ns_prep", ns_prep_vec_kernel<bf16>, dim3(vchunks, nb), dim3(256), 0, st, m, n, L.hd,
+                            L.heads, (const bf16*)G, M, mu, nrm));
+    } else if (dt == DION_F32)
         DION_TRY(launch("ns_prep", ns_prep_kernel<float>, dim3(chunks, nb), dim3(256), 0, st, m, n, L.hd, L.heads,
                         (const float*)G, M, mu, nrm));
     else
@@ -203,6 +240,16 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
         return DION_OK;
     }
     const long long total = (long long)batch * m * n;
+    if (vec8) {
+        const unsigned vchunks = (unsigned)std::min<long long>(cdiv(total / 8, 256 * 2), 65535);
+        if (dt == DION_F32)
+            DION_TRY(launch("ns_finish_tc", ns_finish_vec_kernel<float>, dim3(vchunks), dim3(256), 0, st, batch, m, n,
+                            L.hd, L.heads, (const bf16*)Ya, lp, sy, (float*)O, (float*)X, decay, scale));
+        else
+            DION_TRY(launch("ns_finish_tc", ns_finish_vec_kernel<bf16>, dim3(vchunks), dim3(256), 0, st, batch, m, n,
+                            L.hd, L.heads, (const bf16*)Ya, lp, sy, (bf16*)O, (bf16*)X, decay, scale));
+        return DION_OK;
+    }
     const unsigned fchunks = (unsigned)std::min<long long>(cdiv(total, 256 * 4), 65535);
     if (dt == DION_F32)
         DION_TRY(launch("ns_finish_tc", ns_finish_tc_kernel<float>, dim3(fchunks), dim3(256), 0, st, batch, m, n, L.hd,
