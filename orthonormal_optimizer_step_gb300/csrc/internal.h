@@ -49,6 +49,12 @@ struct CholIn {
     // lower triangle is stored block-major, 8 x 8 block t = bi (bi + 1) / 2 + bj
     // at Sin + b * mstride + 64 t, row-major inside the block (as written by
     // qr_gram_sum_blocks)
+    // d0 (optional): the reference diagonal of the dependent-column test,
+    // d0[b * d0stride + j], when the matrix factored is a Schur complement
+    // (a diagonal block of the blocked factorization): a column is dependent
+    // when its pivot is at most 1e-6 of its original squared norm
+    const float* d0;
+    long long d0stride;
 };
 // Cholesky + inverse of batch r x r Gram matrices (one CTA each); see qr.cu.
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,

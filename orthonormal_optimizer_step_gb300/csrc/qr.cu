@@ -466,6 +466,10 @@ __global__ void __launch_bounds__(512, 1) chol_gj_kernel(int r, const float* Sin
         for (int ii = 0; ii < 8; ++ii)
             if (i0 + ii < r) d0[i0 + ii] = a[ii][ii];
     }
+    if (in.d0) {   // reference diagonal given (a Schur complement is factored)
+        __syncthreads();
+        for (int k = tid; k < r; k += nt) d0[k] = in.d0[(size_t)b * in.d0stride + k];
+    }
     // near-identity Gram: L^{-1} = I - strictly_lower(E) - diag(E)/2 (see chol_inv_kernel)
     float em = 0.f;
     if (own) {

@@ -190,6 +190,15 @@ __global__ void __launch_bounds__(256) qr_sum_blocks_kernel(int r, int nparts, c
     }
 }
 
+// dg[b][i] = S[b](i, i): the original diagonal, the reference of the
+// dependent-column test in every diagonal block of the blocked factorization.
+__global__ void __launch_bounds__(256) qr_diag_kernel(int r, const float* __restrict__ S, float* __restrict__ dg)
+{
+    const int b = blockIdx.y;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < r; i += gridDim.x * blockDim.x)
+        dg[(size_t)b * r + i] = S[(size_t)b * r * r + (size_t)i * r + i];
+}
+
 // Panel of the blocked factorization: rows x w block of S (pitch r, matrix
 // pitch r*r) -> three bf16 terms A3[3b + t] (rows x nb, pitch nb, term pitch
 // r*nb), columns w..nb-1 zero.
@@ -284,11 +293,17 @@ cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const fl
 {
     const int nblk = (int)cdiv(r, nb);
     const long long z3 = 3ll * batch, rr = (long long)r * r, mrp = (long long)m * rp, rrp = (long long)r * rp;
+    float* dg = W;   // batch x r original diagonal (W is otherwise unused here)
+    {
+        cudaError_t e = launch("chol_blk_diag0", qr_diag_kernel, dim3((unsigned)cdiv(r, 256), batch), dim3(256), 0, st, r,
+                               (const float*)S, dg);
+        if (e != cudaSuccess) return e;
+    }
     for (int J = 0; J < nblk; ++J) {
         const int j0 = J * nb, w = std::min(nb, r - j0), rest = r - j0 - w;
         const int bnw = pick_bn_qr(w);
         cudaError_t e = chol_inv_io("chol_blk_diag", batch, w, S + (size_t)j0 * r + j0, 1, S, W, nullptr, ZJ, nb,
-                                    dead + j0, status, st, gate, CholIn{rr, 0, r, r});
+                                    dead + j0, status, st, gate, CholIn{rr, 0, r, r, dg + j0, r});
         if (e != cudaSuccess) return e;
         CUtensorMap tZ;
         if (!tmap_bf16(&tZ, ZJ, nb, w, z3, nb, (long long)w * nb, bnw)) return cudaErrorInvalidValue;

@@ -181,18 +181,19 @@ def test_blocked_factorization_reads_no_stale_workspace():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_device_scalars_follow_schedule_under_graph_replay(dtype):
+@pytest.mark.parametrize("dtype,m,n,r", [(torch.float32, 192, 320, 48), (torch.bfloat16, 192, 320, 48),
+                                         (torch.bfloat16, 640, 512, 300)])
+def test_device_scalars_follow_schedule_under_graph_replay(dtype, m, n, r):
     """dion_step_batched_dev captured once in a CUDA graph and replayed while
     the caller writes a new (mu, lr, weight_decay) into device memory gives the
-    same bits as direct calls with those values passed by value."""
-    g = wl.Group(2, 192, 320)
-    r = 48
+    same bits as direct calls with those values passed by value (rank 300:
+    the wide path, whose update runs in GEMM epilogues)."""
+    g = wl.Group(2, m, n)
     X, M, Q = wl.make_state(g, r, dtype, DEV, seed=41)
     grads = [wl.make_grad(g, 1.0, dtype, DEV, 41, s) for s in range(4)]
     schedule = [(0.9, 0.02, 0.01), (0.9, 0.01, 0.01), (0.8, 0.005, 0.0), (0.95, 0.03, 0.1)]
     ref = [t.clone() for t in (X, M, Q)]
-    ws_ref = od.new_workspace(od.dion_workspace_size(2, 192, 320, r, od.DION_BF16 if dtype == torch.bfloat16
+    ws_ref = od.new_workspace(od.dion_workspace_size(2, m, n, r, od.DION_BF16 if dtype == torch.bfloat16
                                                      else od.DION_F32), DEV)
     for (mu, lr, wd), Gs in zip(schedule, grads):
         od.dion_step_batched(ref[0], Gs, ref[1], ref[2], mu=mu, lr=lr, weight_decay=wd, workspace=ws_ref)
@@ -229,3 +230,29 @@ def test_device_scalars_non_finite_sets_status():
     ws = od.dion_step_batched(X, G, M, Q, hyper=hyper)
     torch.cuda.synchronize()
     assert od.dion_get_status(ws) & 2
+
+
+def test_rank_deficient_gradient_blocked_factorization():
+    """Rank 300 (blocked factorization) on B = G of rank 20: the dependent
+    columns found inside the 128-column diagonal blocks are zeroed and
+    flagged, and the remaining columns are orthonormal.  G is built from +-1
+    factors, so its entries are small integers, exact in bf16, and G has
+    rank 20 exactly (a rounded real low-rank G would not be)."""
+    g = wl.Group(1, 512, 640)
+    r = 300
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    u = torch.randint(0, 2, (512, 20), generator=gen).to(torch.float64) * 2 - 1
+    v = torch.randint(0, 2, (20, 640), generator=gen).to(torch.float64) * 2 - 1
+    G = (u @ v).to(torch.bfloat16).unsqueeze(0).to(DEV)
+    X, M, Q = wl.make_state(g, r, torch.bfloat16, DEV, seed=11)
+    M.zero_()
+    ws = od.dion_step_batched(X, G, M, Q, mu=0.9, lr=0.01, weight_decay=0.0)
+    torch.cuda.synchronize()
+    assert od.dion_get_status(ws) & 1
+    P, _ = od.dion_panels(ws, 1, 512, 640, r, od.DION_BF16)
+    P = f64(P[0])
+    live = np.linalg.norm(P, axis=0) > 0.5
+    assert 1 <= live.sum() <= 20 + 1
+    np.testing.assert_allclose(P[:, live].T @ P[:, live], np.eye(live.sum()), atol=1e-3)
+    assert np.all(np.abs(P[:, ~live]) == 0)
+    assert torch.isfinite(X.float()).all() and torch.isfinite(M).all() and torch.isfinite(Q).all()
