@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, in
 // operand), four columns per thread.
 __global__ void __launch_bounds__(256) dion_qemit_kernel(int n, int r, int rp, int rows,
                                                          const float* __restrict__ R, const float* __restrict__ inv,
-                                                         float* __restrict__ Q, bf16* __restrict__ Q16)
+                                                         float* __restrict__ Q, bf16* __restrict__ Q16, bool qvec)
 {
     const int upr = rp >> 2;
     const int total = rows * upr;                     // rows = batch * n
@@ -884,9 +884,13 @@ __global__ void __launch_bounds__(256) dion_qemit_kernel(int n, int r, int rp, i
         *reinterpret_cast<uint2*>(Q16 + (size_t)row * rp + c) =
             make_uint2(tc::pack_bf16x2(q[0], q[1]), tc::pack_bf16x2(q[2], q[3]));
         float* qo = Q + (size_t)row * r + c;
+        if (qvec) {   // r % 4 == 0 and Q 16-byte aligned: whole quads below r
+            if (c < r) *reinterpret_cast<float4*>(qo) = make_float4(q[0], q[1], q[2], q[3]);
+        } else {
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-            if (c + t < r) qo[t] = q[t];
+            for (int t = 0; t < 4; ++t)
+                if (c + t < r) qo[t] = q[t];
+        }
     }
 }
 
@@ -1016,7 +1020,8 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
     {
         const int rows = batch * n;
         DION_TRY(launch("dion_qemit", dion_qemit_kernel, dim3(grid_for((long long)rows * (rp / 4))), dim3(256), 0, st,
-                        n, r, rp, rows, (const float*)R, (const float*)inv, Q, Q16));
+                        n, r, rp, rows, (const float*)R, (const float*)inv, Q, Q16,
+                        (r % 4) == 0 && ((uintptr_t)Q & 15u) == 0));
     }
     // 9. M and X updates
     CUtensorMap tmPa, tmR, tmQ;

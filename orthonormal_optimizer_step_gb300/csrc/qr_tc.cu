@@ -89,33 +89,71 @@ __global__ void __launch_bounds__(256) qr_split_kernel(int m, int r, int rp, con
 // matrix; the factorization then runs only for matrices with max|E| above
 // kNearIdentityTol (overwriting these terms).  Only the lower triangle of S is
 // read (S is symmetric; the blocked path computes only that half).
+template <bool V4>
 __global__ void __launch_bounds__(256) qr_near_identity_kernel(int r, int ldz, const float* __restrict__ S6,
                                                                int nparts, bf16* __restrict__ Z3, int* emax)
 {
+    // V4: four consecutive columns per thread (r and ldz multiples of 4): one
+    // 16-byte load per partial and one 8-byte store per term
+    constexpr int kW = V4 ? 4 : 1;
     const int b = blockIdx.y;
     const size_t rr = (size_t)r * r, zs = (size_t)r * ldz;
     const float* Sb = S6 + (size_t)b * nparts * rr;
     bf16* z0 = Z3 + (size_t)3 * b * zs;
     float em = 0.f;
-    const int total = r * ldz;
+    const int upr = ldz / kW, total = r * upr;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
-        const int i = e / ldz, k = e - i * ldz;
-        float v = 0.f;
-        if (k <= i) {
-            const size_t o = (size_t)i * r + k;
-            float sv = 0.f;
+        const int i = e / upr, k0 = (e - i * upr) * kW;
+        float sv[kW];
 #pragma unroll
-            for (int q = 0; q < 6; ++q)
-                if (q < nparts) sv += Sb[q * rr + o];
-            const float ev = sv - (i == k ? 1.f : 0.f);
-            em = fmaxf(em, isfinite(ev) ? fabsf(ev) : 1e30f);
-            v = (k < i) ? -sv : 1.f - 0.5f * ev;
+        for (int t = 0; t < kW; ++t) sv[t] = 0.f;
+        if (k0 <= i) {
+            const size_t o = (size_t)i * r + k0;
+            if constexpr (V4) {
+#pragma unroll
+                for (int q = 0; q < 6; ++q)
+                    if (q < nparts) {
+                        const float4 x = __ldg(reinterpret_cast<const float4*>(Sb + q * rr + o));
+                        sv[0] += x.x; sv[1] += x.y; sv[2] += x.z; sv[3] += x.w;
+                    }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 6; ++q)
+                    if (q < nparts) sv[0] += Sb[q * rr + o];
+            }
         }
-        bf16 h1, h2, h3;
-        split3(v, h1, h2, h3);
-        z0[e] = h1;
-        z0[zs + e] = h2;
-        z0[2 * zs + e] = h3;
+        float v[kW];
+#pragma unroll
+        for (int t = 0; t < kW; ++t) {
+            const int k = k0 + t;
+            v[t] = 0.f;
+            if (k <= i) {
+                const float ev = sv[t] - (i == k ? 1.f : 0.f);
+                em = fmaxf(em, isfinite(ev) ? fabsf(ev) : 1e30f);
+                v[t] = (k < i) ? -sv[t] : 1.f - 0.5f * ev;
+            }
+        }
+        const size_t zo = (size_t)i * ldz + k0;
+        if constexpr (V4) {
+            uint32_t w[3][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                bf16 a1, a2, a3, c1, c2, c3;
+                split3(v[2 * h], a1, a2, a3);
+                split3(v[2 * h + 1], c1, c2, c3);
+                w[0][h] = (uint32_t)__bfloat16_as_ushort(a1) | ((uint32_t)__bfloat16_as_ushort(c1) << 16);
+                w[1][h] = (uint32_t)__bfloat16_as_ushort(a2) | ((uint32_t)__bfloat16_as_ushort(c2) << 16);
+                w[2][h] = (uint32_t)__bfloat16_as_ushort(a3) | ((uint32_t)__bfloat16_as_ushort(c3) << 16);
+            }
+#pragma unroll
+            for (int q = 0; q < 3; ++q) *reinterpret_cast<uint2*>(z0 + q * zs + zo) = make_uint2(w[q][0], w[q][1]);
+        } else {
+            bf16 h1, h2, h3;
+            split3(v[0], h1, h2, h3);
+            z0[zo] = h1;
+            z0[zs + zo] = h2;
+            z0[2 * zs + zo] = h3;
+        }
     }
     for (int o = 16; o > 0; o >>= 1) em = fmaxf(em, __shfl_xor_sync(0xffffffffu, em, o));
     if ((threadIdx.x & 31) == 0) atomicMax(&emax[b], __float_as_int(em));   // em >= 0: int order = float order
@@ -166,6 +204,7 @@ __global__ void __launch_bounds__(256) qr_sum_blocks_kernel(int r, int nparts, c
     const size_t rr = (size_t)r * r;
     const float* src = S6 + (size_t)b * nparts * rr;
     float* dst = Sblk + (size_t)b * sblk;
+    const bool vec = (r % 4) == 0 && ((uintptr_t)S6 & 15u) == 0;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < tot4;
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e >> 4), q = (int)(e & 15), ii = q >> 1, j0 = (q & 1) * 4;
@@ -175,16 +214,32 @@ __global__ void __launch_bounds__(256) qr_sum_blocks_kernel(int r, int nparts, c
         const int bj = t - bi * (bi + 1) / 2;
         const int i = bi * 8 + ii, j = bj * 8 + j0;
         float v[4];
+        if (vec && i < r && j + 3 <= i) {   // whole quad in the lower triangle: one 16-byte load per partial
+            const size_t o = (size_t)i * r + j;
+            float4 x[6];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int jj = j + u;
-            float x = (i == jj && i >= r) ? 1.f : 0.f;
-            if (i < r && jj <= i) {
-                const size_t o = (size_t)i * r + jj;
-                x = src[o];
-                for (int p = 1; p < nparts; ++p) x += src[p * rr + o];
+            for (int p = 0; p < 6; ++p)
+                if (p < nparts) x[p] = __ldg(reinterpret_cast<const float4*>(src + p * rr + o));
+            v[0] = x[0].x; v[1] = x[0].y; v[2] = x[0].z; v[3] = x[0].w;
+#pragma unroll
+            for (int p = 1; p < 6; ++p)
+                if (p < nparts) {
+                    v[0] += x[p].x; v[1] += x[p].y; v[2] += x[p].z; v[3] += x[p].w;
+                }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int jj = j + u;
+                float x = (i == jj && i >= r) ? 1.f : 0.f;
+                if (i < r && jj <= i) {
+                    const size_t o = (size_t)i * r + jj;
+                    x = src[o];
+#pragma unroll
+                    for (int p = 1; p < 6; ++p)
+                        if (p < nparts) x += src[p * rr + o];
+                }
+                v[u] = x;
             }
-            v[u] = x;
         }
         reinterpret_cast<float4*>(dst)[e] = make_float4(v[0], v[1], v[2], v[3]);
     }
@@ -443,10 +498,12 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
             // near-identity inverse on all SMs; the factorization runs only where it does not apply
             e = cudaMemsetAsync(emax, 0, sizeof(int) * batch, st);
             if (e != cudaSuccess) return e;
-            const long long tot = (long long)r * rp;
-            e = launch("qr_near_identity", qr_near_identity_kernel,
-                       dim3((unsigned)std::min<long long>(cdiv(tot, 1024), 1024), batch), dim3(256), 0, st, r, rp,
-                       (const float*)(direct ? S : S6), direct ? 1 : 6, Z3, emax);
+            const float* Sn = direct ? S : S6;
+            const bool v4 = (r % 4) == 0 && (rp % 4) == 0 && ((uintptr_t)Sn & 15u) == 0;
+            const long long units = (long long)r * rp / (v4 ? 4 : 1);
+            e = launch("qr_near_identity", v4 ? qr_near_identity_kernel<true> : qr_near_identity_kernel<false>,
+                       dim3((unsigned)std::min<long long>(cdiv(units, 256), 1024), batch), dim3(256), 0, st, r, rp, Sn,
+                       direct ? 1 : 6, Z3, emax);
             if (e != cudaSuccess) return e;
         }
         const int* gate = pass == 1 ? emax : nullptr;
