@@ -357,10 +357,10 @@ def run_gb300(args, rank, world, local_rank):
         h2d = sum(t.numel() * t.element_size() for t in hostG)
         d2h = sum(t.numel() * t.element_size() for t in hostX)
 
-        # Each shape group is stepped as two half-batch calls on their own
-        # streams (the matrices are independent), so that the first half's
-        # step and weight copy-out overlap the second half's gradient copy-in.
-        nsplit = 2
+        # Each shape group is stepped as --e2e-parts calls (two by default) on
+        # their own streams (the matrices are independent), so that one part's
+        # step and weight copy-out overlap the next part's gradient copy-in.
+        nsplit = max(1, args.e2e_parts)
         parts = []
         for st, hg, hx in zip(state, hostG, hostX):
             B = st["g"].batch
@@ -477,6 +477,8 @@ def main():
     ap.add_argument("--skip-muon", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--e2e-parts", type=int, default=2,
+                    help="calls per shape group in the end-to-end run (each on its own stream)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--one-stream", dest="group_streams", action="store_false",
                     help="run the shape groups one after another on one stream")
