@@ -34,9 +34,10 @@
  *   - Argument errors (shape, null pointer, alignment, dtype, workspace too
  *     small) are detected on the host and returned before anything is
  *     enqueued.  A failed kernel launch returns DION_ERR_CUDA.
- *   - Numeric breakdown found on the device (a non-positive Cholesky pivot in
- *     the orthonormalization of P, i.e. P is rank deficient, or a non-finite
- *     value) does not trap: it is recorded in a status word inside the
+ *   - Numeric breakdown found on the device (a Cholesky pivot in the
+ *     orthonormalization of P at most 1e-6 times its column's squared norm,
+ *     i.e. P is rank deficient to that tolerance, or a non-finite value)
+ *     does not trap: it is recorded in a status word inside the
  *     workspace, read with dion_get_status after the caller has synchronized
  *     the stream.  Columns of P found dependent are set to zero, so the step
  *     still completes with finite output at a lower rank.
@@ -201,8 +202,8 @@ dion_status muon_ns_batched(int batch, int m, int n, int head_dim, dion_dtype dt
  * Reads the device status word of a workspace used by dion_step_batched or
  * muon_ns_batched (a blocking device-to-host copy of 4 bytes; synchronize
  * the stream of the last call first).  *device_status = 0 means no numeric
- * breakdown; otherwise a bit set: 1 = non-positive Cholesky pivot (rank-
- * deficient P), 2 = non-finite value met.  The word is cleared at the start
+ * breakdown; otherwise a bit set: 1 = a Cholesky pivot at most 1e-6 times
+ * its column's squared norm (rank-deficient P), 2 = non-finite value met.  The word is cleared at the start
  * of every step.  Returns DION_ERR_NUMERIC when the word is non-zero.
  */
 dion_status dion_get_status(const void* workspace, int* device_status);
