@@ -180,6 +180,25 @@ def alu_peak_tflops(sm_mhz=2070.0, sms=152):
 
 # ----------------------------------------------------------------- arms
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank contributes its own timed region
+    and all ranks receive the maximum (a no-op for one rank)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ms_per_step, world):
+    """Whole-job time per megabatch: each of the world replicas steps its own
+    megabatch in ms_per_step (the max over ranks), so the job advances world
+    megabatches in that time."""
+    return ms_per_step / max(1, world)
+
+
 def run_gb300(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -240,12 +259,7 @@ def run_gb300(args, rank, world, local_rank):
         if prof is not None:
             prof.__exit__(None, None, None)
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                     if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
@@ -390,7 +404,7 @@ def run_gb300(args, rank, world, local_rank):
             e2e_step()
         esteps = max(1, args.steps // 2)
         ems = timed(e2e_step, esteps) / esteps
-        e2e = {"value": ems / world, "unit": "ms", "ms_per_step": ems, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(ems, world), "unit": "ms", "ms_per_step": ems, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "calls_per_group": nsplit}
 
     # --- CPU baseline: the oracle on a bounded sample ---
@@ -399,7 +413,7 @@ def run_gb300(args, rank, world, local_rank):
         cpu = cpu_baseline(w, budget_s=args.cpu_budget)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": ms_step / world, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        line = {"metric": METRIC, "value": job_value(ms_step, world), "unit": "ms", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic (seeded Gaussian, workloads/)",
