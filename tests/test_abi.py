@@ -66,6 +66,13 @@ def test_step_rejects_bad_arguments_before_launch(lib):
     big = ctypes.c_size_t(1 << 40)
     fake = ctypes.c_void_p(1 << 20)        # never dereferenced: validation fails first
     ws = ctypes.c_void_p(1 << 24)
+    # empty megabatch or empty matrices
+    for (b, m, n) in [(0, 64, 64), (1, 0, 64), (1, 64, 0), (-1, 64, 64)]:
+        assert lib.dion_step_batched(b, m, n, 1, 0, fake, fake, fake, fake, 0.9, 0.01, 0.0, ws, big, None) \
+            == od.DION_ERR_INVALID_ARG
+        assert lib.muon_ns_batched(b, m, n, 0, 1, fake, fake, None, None, 5,
+                                   (ctypes.c_float * 3)(3.4445, -4.775, 2.0315), 0.9, 0.01, 0.0, ws, big, None) \
+            == od.DION_ERR_INVALID_ARG
     # null pointers
     assert lib.dion_step_batched(1, 64, 64, 8, 0, None, fake, fake, fake, 0.9, 0.01, 0.0, ws, big, None) \
         == od.DION_ERR_INVALID_ARG
