@@ -93,6 +93,43 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------ DRAM traffic from ncu
+
+def csrc_digest():
+    """sha256 over libdion's sources: a DRAM-traffic figure captured with other
+    sources no longer describes the kernel and is not reported."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "orthonormal_optimizer_step_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(src, "*"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the
+    committed summary profiles/dram_traffic_<workload>.txt (lines
+    "launch <i> <kernel> read_bytes <r> write_bytes <w>" and
+    "csrc_sha256 <hex>"), or (None, why)."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None, "no capture for this workload"
+    digest, vals = None, []
+    for ln in open(path):
+        f = ln.split()
+        if len(f) >= 2 and f[0] == "csrc_sha256":
+            digest = f[1]
+        if len(f) >= 7 and f[0] == "launch" and f[2] == kernel:
+            vals.append(float(f[4]) + float(f[6]))
+    if not vals:
+        return None, f"no launches of {kernel} in {os.path.basename(path)}"
+    if digest != csrc_digest():
+        return None, "kernel sources changed since the capture"
+    return sum(vals) / len(vals), f"profiles/{os.path.basename(path)} ({len(vals)} launches)"
+
+
 # ----------------------------------------------------------- workload setup
 
 def build_state(w, device, seed0):
@@ -207,7 +244,7 @@ def run_gb300(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = wl.WORKLOADS[args.workload]()
+    w = select_groups(wl.WORKLOADS[args.workload](), args.group, args.fraction)
     pk = peaks()
     state = build_state(w, dev, 1000 + 17 * rank)
     for st in state:
@@ -264,58 +301,67 @@ def run_gb300(args, rank, world, local_rank):
     clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                     if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
 
-    # --- Dion (headline): groups on their own streams, no per-kernel events
-    for _ in range(args.warmup):
-        dion_step()
-    clocks.start()
-    ms = timed(dion_step, args.steps)
-    ms_step = ms / args.steps
-    # --- the same steps again, one group after another on one stream, with an
-    # event pair around every libdion kernel: per-kernel device times for the
-    # roofline (kernels of different groups do not share the GPU here)
-    saved_streams = list(streams)
-    streams[:] = [main for _ in state]
-    prof = od.profile(max_launches=2048 * args.steps * len(state) + 64)
-    ms_seq = timed(dion_step, args.steps, prof) / args.steps
-    torch.cuda.synchronize()
-    streams[:] = saved_streams
-    kernels = prof.read()
-    gpu_launches = sum(v[0] for v in kernels.values())   # the headline region launches the same kernels
-    by, fl = 0, 0.0
-    eb = 2 if w.dtype == torch.bfloat16 else 4
-    for st in state:
-        b, f = dion_bytes_flops(st["g"], st["r"], eb)
-        by += b
-        fl += f
-    # dominant kernel by device time
-    dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else (None, (0, 0.0))
-    dom_name, (dom_launches, dom_ms) = dom
-    bound, cost_step = kernel_cost(dom_name or "", w, state)
-    per_launch_ms = dom_ms / max(dom_launches, 1)
-    achieved, peak, unit = None, None, None
-    if bound and dom_ms > 0:
-        rate = cost_step * args.steps / (dom_ms * 1e-3)
-        if bound == "hbm":
-            achieved, peak, unit = rate / 1e9, pk["hbm_gbs"], "GB/s"
-        elif bound == "tensor":
-            achieved, peak, unit = rate / 1e12, pk["bf16_tflops"], "TFLOP/s"
-        else:
-            achieved, peak, unit = rate / 1e12, alu_peak_tflops(), "TFLOP/s"
-    # every streaming kernel's own fraction, for context
-    per_kernel = {}
-    for k, (nl, kms) in kernels.items():
-        kb, kc = kernel_cost(k, w, state)
-        if kb == "hbm" and kms > 0:
-            per_kernel[k] = round(kc * args.steps / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
-    roofline = {"bound": bound or "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": (achieved / peak) if achieved and peak else None, "traffic": None,
-                "peak_source": pk["source"] if bound != "alu" else "derived: 152 SMs x 128 FMA x 2 x 2070 MHz",
-                "launches": dom_launches, "ms_per_launch": per_launch_ms,
-                "hbm_frac_by_kernel": per_kernel,
-                "step_hbm_floor_ms": by / (pk["hbm_gbs"] * 1e9) * 1e3,
-                "step_tensor_floor_ms": fl / (pk["bf16_tflops"] * 1e12) * 1e3,
-                "step_frac_of_floor": max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)) * 1e3
-                / ms_step}
+    if args.skip_dion:   # Newton-Schulz only (profiling captures of its GEMM chain)
+        clocks.start()
+        ms_step = ms_seq = None
+        kernels, gpu_launches, roofline, by, fl = {}, 0, None, 0, 0.0
+    else:
+        # --- Dion (headline): groups on their own streams, no per-kernel events
+        for _ in range(args.warmup):
+            dion_step()
+        clocks.start()
+        ms = timed(dion_step, args.steps)
+        ms_step = ms / args.steps
+        # --- the same steps again, one group after another on one stream, with an
+        # event pair around every libdion kernel: per-kernel device times for the
+        # roofline (kernels of different groups do not share the GPU here)
+        saved_streams = list(streams)
+        streams[:] = [main for _ in state]
+        prof = od.profile(max_launches=2048 * args.steps * len(state) + 64)
+        ms_seq = timed(dion_step, args.steps, prof) / args.steps
+        torch.cuda.synchronize()
+        streams[:] = saved_streams
+        kernels = prof.read()
+        gpu_launches = sum(v[0] for v in kernels.values())   # the headline region launches the same kernels
+        by, fl = 0, 0.0
+        eb = 2 if w.dtype == torch.bfloat16 else 4
+        for st in state:
+            b, f = dion_bytes_flops(st["g"], st["r"], eb)
+            by += b
+            fl += f
+        # dominant kernel by device time
+        dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else (None, (0, 0.0))
+        dom_name, (dom_launches, dom_ms) = dom
+        bound, cost_step = kernel_cost(dom_name or "", w, state)
+        per_launch_ms = dom_ms / max(dom_launches, 1)
+        achieved, peak, unit = None, None, None
+        if bound and dom_ms > 0:
+            rate = cost_step * args.steps / (dom_ms * 1e-3)
+            if bound == "hbm":
+                achieved, peak, unit = rate / 1e9, pk["hbm_gbs"], "GB/s"
+            elif bound == "tensor":
+                achieved, peak, unit = rate / 1e12, pk["bf16_tflops"], "TFLOP/s"
+            else:
+                achieved, peak, unit = rate / 1e12, alu_peak_tflops(), "TFLOP/s"
+        # every streaming kernel's own fraction, for context
+        per_kernel = {}
+        for k, (nl, kms) in kernels.items():
+            kb, kc = kernel_cost(k, w, state)
+            if kb == "hbm" and kms > 0:
+                per_kernel[k] = round(kc * args.steps / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
+        traffic, traffic_src = profiled_traffic(w.name, dom_name) if dom_name else (None, "no kernel")
+        roofline = {"bound": bound or "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": unit,
+                    "frac": (achieved / peak) if achieved and peak else None, "traffic": traffic,
+                    "traffic_unit": "bytes per launch (dram read + write, ncu)", "traffic_source": traffic_src,
+                    "algorithmic_bytes_per_launch": cost_step / max(dom_launches / args.steps, 1) if bound == "hbm"
+                    else None,
+                    "peak_source": pk["source"] if bound != "alu" else "derived: 152 SMs x 128 FMA x 2 x 2070 MHz",
+                    "launches": dom_launches, "ms_per_launch": per_launch_ms,
+                    "hbm_frac_by_kernel": per_kernel,
+                    "step_hbm_floor_ms": by / (pk["hbm_gbs"] * 1e9) * 1e3,
+                    "step_tensor_floor_ms": fl / (pk["bf16_tflops"] * 1e12) * 1e3,
+                    "step_frac_of_floor": max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)) * 1e3
+                    / ms_step}
 
     # --- Muon / Newton-Schulz comparison path ---
     muon = None
@@ -353,13 +399,17 @@ def run_gb300(args, rank, world, local_rank):
         gemm_ms = sum(v[1] for k, v in mk.items() if k.startswith("ns_") and ("gram" in k or "poly" in k
                                                                               or "axpy" in k))
         ach = nfl / (gemm_ms / msteps * 1e-3) / 1e12 if gemm_ms > 0 else None
+        # the GEMM chain runs back to back for the whole timed region: past about
+        # a second of it the GPU sits at its power cap, so the sustained peak applies
+        sustained = mms * msteps >= 1000.0
+        npk = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
         muon = {"ms_per_step": mms, "group_streams": bool(mms_streams <= mms_seq),
                 "ms_per_step_streams": mms_streams, "ms_per_step_one_stream": mms_seq,
                 "tflops_step": nfl / (mms * 1e-3) / 1e12,
                 "roofline": {"bound": "tensor", "kernel": "ns gemm chain", "achieved": ach,
-                             "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                             "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,
-                             "peak_source": pk["source"]},
+                             "peak": npk, "unit": "TFLOP/s",
+                             "frac": ach / npk if ach else None, "traffic": None,
+                             "peak_source": pk["source"] + (" sustained" if sustained else " burst")},
                 "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in mk.items()}}
     clk = clocks.stop()
 
@@ -413,7 +463,7 @@ def run_gb300(args, rank, world, local_rank):
         cpu = cpu_baseline(w, budget_s=args.cpu_budget)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": job_value(ms_step, world), "unit": "ms", "n_gpus": world, "steps": args.steps,
+        line = {"metric": METRIC, "value": job_value(ms_step, world) if ms_step is not None else None, "unit": "ms", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic (seeded Gaussian, workloads/)",
@@ -429,54 +479,102 @@ def run_gb300(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, budget_s=20.0, seed=5):
-    """Times the oracle (as it stands) on one matrix per shape group for one
-    Dion step, and extrapolates to a megabatch step by the batch counts."""
+def _oracle_inputs(w, g, rng):
     import numpy as np
-    import oracle
+    r = g.rank(w.fraction)
+    X = 0.02 * rng.standard_normal((g.m, g.n))
+    G = w.g_std * rng.standard_normal((g.m, g.n))
+    M = w.g_std * rng.standard_normal((g.m, g.n))
+    Q = rng.standard_normal((g.n, r))
+    Q /= np.linalg.norm(Q, axis=0)
+    return X, G, M, Q
+
+
+def oracle_megabatch_ms(w, budget_s, seed=5):
+    """Times the oracle's dense-library form (numpy products and LAPACK QR in
+    float64, as it stands) on the host cores for one Dion step of the
+    workload.  One matrix per shape group is timed first; when the whole
+    megabatch fits in budget_s by that estimate, it is then timed in full,
+    else the per-group times are scaled by the batch counts (extrapolated).
+    Returns (ms per megabatch, ms actually timed, sample description,
+    extrapolated)."""
+    import numpy as np
+    import oracle.dense as dense
     rng = np.random.default_rng(seed)
-    total_ms = 0.0
-    sample = []
-    t_start = time.time()
+    per = []
     for g in w.groups:
-        r = g.rank(w.fraction)
-        X = (0.02 * rng.standard_normal((g.m, g.n)))
-        G = w.g_std * rng.standard_normal((g.m, g.n))
-        M = np.zeros((g.m, g.n))
-        Q = rng.standard_normal((g.n, r))
-        Q /= np.linalg.norm(Q, axis=0)
+        ins = _oracle_inputs(w, g, rng)
         t0 = time.perf_counter()
-        oracle.dion_step(X, G, M, Q, w.mu, w.lr, w.wd)
-        dt = (time.perf_counter() - t0) * 1e3
-        total_ms += dt * g.batch
-        sample.append(f"1x{g.m}x{g.n} r={r}")
-        if time.time() - t_start > budget_s:
-            return {"value": None, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
-                    "sample": "budget exceeded after " + ", ".join(sample)}
-    return {"value": total_ms, "unit": "ms", "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count())),
-            "kind": "oracle",
-            "sample": "one matrix per shape group (" + ", ".join(sample) + "), one Dion step each, "
-                      "scaled by the batch counts to one megabatch step"}
+        dense.dion_step(*ins, w.mu, w.lr, w.wd)
+        per.append((time.perf_counter() - t0) * 1e3)
+    one = sum(per)
+    est = sum(g.batch * t for g, t in zip(w.groups, per))
+    if est <= budget_s * 1e3:
+        t0 = time.perf_counter()
+        for g in w.groups:
+            for _ in range(g.batch):
+                dense.dion_step(*_oracle_inputs(w, g, rng), w.mu, w.lr, w.wd)
+        full = (time.perf_counter() - t0) * 1e3
+        return full, full + one, "the whole megabatch (" + ", ".join(
+            f"{g.batch}x{g.m}x{g.n} r={g.rank(w.fraction)}" for g in w.groups) + "), one Dion step", False
+    return est, one, "one matrix per shape group (" + ", ".join(
+        f"1x{g.m}x{g.n} r={g.rank(w.fraction)}" for g in w.groups) + "), one Dion step each; the megabatch " \
+        "value is extrapolated by the batch counts (" + ", ".join(str(g.batch) for g in w.groups) + ")", True
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(w, budget_s=30.0, seed=5):
+    """The oracle on the host cores, on a bounded sample of the workload."""
+    ms, timed_ms, sample, extrap = oracle_megabatch_ms(w, budget_s, seed)
+    return {"value": ms, "unit": "ms", "cores": host_cores(), "kind": "oracle",
+            "form": "dense-library form (numpy/LAPACK, float64)", "sample": sample, "extrapolated": extrap,
+            "timed_ms": timed_ms}
+
+
+def select_groups(w, groups, fraction=None):
+    """The workload restricted to the shape groups listed (all if None), at
+    another rank fraction if one is given."""
+    import dataclasses
+    if fraction is not None:
+        w = dataclasses.replace(w, name=f"{w.name}@r{fraction:g}", fraction=float(fraction))
+    if not groups:
+        return w
+    return dataclasses.replace(w, name=w.name + "[" + ",".join(str(g) for g in groups) + "]",
+                               groups=tuple(w.groups[g] for g in groups))
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the oracle itself, on the host cores."""
+    """The reference arm: the oracle itself, on the host cores.  Each step is
+    one bounded sample of the workload (the whole megabatch when it fits the
+    per-step budget, else one matrix per shape group, extrapolated by the batch
+    counts)."""
     if rank != 0:
         return
     import workloads as wl
-    w = wl.WORKLOADS[args.workload]()
+    w = select_groups(wl.WORKLOADS[args.workload](), args.group, args.fraction)
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=1e9)
-    vals = []
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(w, budget_s=1e9)["value"])
+        oracle_megabatch_ms(w, args.cpu_budget)
+    vals, timed = [], []
+    sample, extrap = "", False
+    for k in range(args.steps):
+        v, t, sample, extrap = oracle_megabatch_ms(w, args.cpu_budget, seed=5 + k)
+        vals.append(v)
+        timed.append(t)
     ms = statistics.mean(vals)
-    cb = cpu_baseline(w, budget_s=1e9)
-    cb["value"] = ms
+    cb = {"value": ms, "unit": "ms", "cores": host_cores(), "kind": "oracle",
+          "form": "dense-library form (numpy/LAPACK, float64)", "sample": sample, "extrapolated": extrap,
+          "timed_ms_per_step": statistics.mean(timed)}
     line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Gaussian)",
-            "config": {"workload": w.name}, "cpu_baseline": cb,
+            "config": {"workload": w.name}, "cpu_baseline": cb, "extrapolated": extrap,
+            "timed_ms_per_step": statistics.mean(timed),
             "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -487,13 +585,22 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="gpt-small-megabatch")
+    ap.add_argument("--workload", default="llama3-8b-megabatch",
+                    help="workload name (workloads.WORKLOADS); default: the Llama-3-8B megabatch, the largest "
+                         "single-GPU workload")
+    ap.add_argument("--group", type=int, action="append", default=None,
+                    help="run only this shape group of the workload (repeatable; for profiling captures)")
+    ap.add_argument("--fraction", type=float, default=None,
+                    help="override the workload's Dion rank fraction (for profiling captures)")
+    ap.add_argument("--skip-dion", action="store_true",
+                    help="time only the Newton-Schulz path (no Dion line; for profiling captures)")
     ap.add_argument("--skip-muon", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--e2e-parts", type=int, default=2,
                     help="calls per shape group in the end-to-end run (each on its own stream)")
-    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--cpu-budget", type=float, default=30.0,
+                    help="seconds of oracle time for the CPU baseline (and per reference-arm step)")
     ap.add_argument("--one-stream", dest="group_streams", action="store_false",
                     help="run the shape groups one after another on one stream")
     args = ap.parse_args()

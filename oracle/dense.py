@@ -95,3 +95,47 @@ def muon_step(X, G, M, *, head_dim=0, steps=5, coeff=QUINTIC, eps=NS_EPS, mu=0.9
                             for h in range(0, n, head_dim)], axis=1)
     X_new = None if X is None else (1.0 - lr * wd) * _f64(X) - (lr * np.sqrt(m / n)) * O
     return {"O": O, "X": X_new, "M": M_new}
+
+
+def newton_schulz_rows(Y, rows, steps=5, coeff=QUINTIC, eps=NS_EPS):
+    """Rows `rows` of newton_schulz(Y), computed without forming the other rows.
+
+    With Y0 the normalized short-side matrix (s x l) and A_k = Y_k Y_k^T, each
+    step is Y_{k+1} = p(A_k) Y_k with p(x) = a + b x + c x^2, so
+    A_{k+1} = A_k p(A_k)^2, every A_k is a polynomial in A_0 (they commute),
+    and the result is p(A_{K-1}) ... p(A_0) Y0.  A product with A_k is
+    evaluated through that recursion (one product with A_k costs five with
+    A_{k-1}), on a few vectors at a time: each step of the iteration applied
+    as written, to the sampled rows (short side) or columns (long side) only.
+    Cost: one s x s Gram matrix plus 2 (1 + 5 + ... + 5^(K-1)) products of it
+    with a thin block."""
+    Y = _f64(Y)
+    m, n = Y.shape
+    rows = np.asarray(rows, dtype=np.int64)
+    tr = m > n
+    Y0 = Y.T if tr else Y                       # s x l, s = min(m, n)
+    Y0 = Y0 / (np.linalg.norm(Y0) + eps)
+    A0 = Y0 @ Y0.T
+    a, b, c = coeff
+
+    def apply_A(k, V):                          # A_k V
+        if k == 0:
+            return A0 @ V
+        return apply_A(k - 1, apply_p(k - 1, apply_p(k - 1, V)))
+
+    def apply_p(k, V):                          # p(A_k) V
+        AV = apply_A(k, V)
+        return a * V + b * AV + c * apply_A(k, AV)
+
+    if tr:
+        # rows of O are columns of the final s x l iterate: p-chain on Y0's columns
+        V = np.ascontiguousarray(Y0[:, rows])
+        for k in range(int(steps)):
+            V = apply_p(k, V)
+        return np.ascontiguousarray(V.T)
+    # rows of O are rows of the final iterate: (p-chain e_i)^T Y0 (symmetric, commuting factors)
+    E = np.zeros((Y0.shape[0], rows.size))
+    E[rows, np.arange(rows.size)] = 1.0
+    for k in range(int(steps)):
+        E = apply_p(k, E)
+    return np.ascontiguousarray(E.T @ Y0)

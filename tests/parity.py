@@ -34,46 +34,84 @@ def storage_round(x, dtype):
     return oracle.round_bf16(x) if dtype == torch.bfloat16 else oracle.round_f32(x)
 
 
-def dion_pair(X, G, M, Q, mu, lr, wd, samples=None):
+def rel_outer(A, B, C, D) -> float:
+    """||A B^T - C D^T||_F / ||C D^T||_F from r x r products only:
+    ||A B^T - C D^T||_F^2 = <A^T A, B^T B> - 2 <A^T C, B^T D> + <C^T C, D^T D>."""
+    aa, bb, cc, dd = A.T @ A, B.T @ B, C.T @ C, D.T @ D
+    num = np.sum(aa * bb) - 2.0 * np.sum((A.T @ C) * (B.T @ D)) + np.sum(cc * dd)
+    den = np.sum(cc * dd)
+    return float(np.sqrt(max(num, 0.0) / (den if den > 0 else 1.0)))
+
+
+def dion_snapshot(X, G, M, Q, samples=None):
+    """float64 host copies of the state of the sampled matrices (default: all)."""
+    idx = list(range(X.shape[0])) if samples is None else list(samples)
+    return idx, {k: f64(t[idx]) for k, t in (("X", X), ("G", G), ("M", M), ("Q", Q))}
+
+
+def dion_pair(X, G, M, Q, mu, lr, wd, samples=None, form=oracle):
     """Run one GPU Dion step (in place on X, M, Q) and the oracle on copies of
-    the same state for the matrices in `samples` (default: all).  Returns a
-    dict of per-quantity worst relative errors and the GPU status."""
+    the same state for the matrices in `samples` (default: all).  `form` is
+    the oracle form (the C triple loops, or oracle.dense for full-size
+    matrices).  Returns a dict of per-quantity worst relative errors and the
+    GPU status."""
+    idx, host = dion_snapshot(X, G, M, Q, samples)
+    ws = od.dion_step_batched(X, G, M, Q, mu=mu, lr=lr, weight_decay=wd)
+    torch.cuda.synchronize()
+    return dion_compare(idx, host, X, M, Q, ws, mu, lr, wd, form)
+
+
+def dion_compare(idx, host, X, M, Q, ws, mu, lr, wd, form=oracle):
+    """Compares the GPU state after a completed step (X, M, Q and the panels P,
+    R left in the workspace ws) with the oracle run from the snapshot `host`."""
     batch, m, n = X.shape
     r = Q.shape[-1]
     dt = X.dtype
-    idx = list(range(batch)) if samples is None else list(samples)
-    host = {k: f64(t[idx]) for k, t in (("X", X), ("G", G), ("M", M), ("Q", Q))}
-    ws = od.dion_step_batched(X, G, M, Q, mu=mu, lr=lr, weight_decay=wd)
-    torch.cuda.synchronize()
     status = od.dion_get_status(ws)
     P_gpu, R_gpu = od.dion_panels(ws, batch, m, n, r, od.DION_BF16 if dt == torch.bfloat16 else od.DION_F32)
-    out = {"M": 0.0, "Q": 0.0, "X": 0.0, "PQt": 0.0, "orth": 0.0, "R": 0.0, "x_ulps": 0.0}
+    out = {"M": 0.0, "Q": 0.0, "X": 0.0, "PQt": 0.0, "orth": 0.0, "R": 0.0, "x_ulps": 0.0, "qcol": 0.0}
     for k, b in enumerate(idx):
-        o = oracle.dion_step(host["X"][k], host["G"][k], host["M"][k], host["Q"][k], mu, lr, wd)
+        o = form.dion_step(host["X"][k], host["G"][k], host["M"][k], host["Q"][k], mu, lr, wd)
         Pg, Rg, Qg = f64(P_gpu[b]), f64(R_gpu[b]), f64(Q[b])
         out["M"] = max(out["M"], rel(f64(M[b]), o["M"]))
         out["Q"] = max(out["Q"], rel(sign_align(Qg, o["Q"]), o["Q"]))
         out["R"] = max(out["R"], rel(sign_align(Rg, o["R"]), o["R"]))
-        out["PQt"] = max(out["PQt"], rel(Pg @ Qg.T, o["P"] @ o["Q"].T))
+        out["PQt"] = max(out["PQt"], rel_outer(Pg, Qg, o["P"], o["Q"]))
         out["orth"] = max(out["orth"], float(np.abs(Pg.T @ Pg - np.eye(r)).max()))
-        Xo = storage_round(o["X"], dt)
+        # the GPU's own Q' is its own R with unit-norm columns (zero columns stay zero)
+        nr = np.linalg.norm(Rg, axis=0)
+        out["qcol"] = max(out["qcol"], float(np.abs(Qg - Rg / np.where(nr > 0, nr, 1.0)).max()))
+        x0 = host["X"][k]
         Xg = f64(X[b])
-        dX_o = Xo - host["X"][k]
-        dX_g = Xg - host["X"][k]
-        out["X"] = max(out["X"], rel(dX_g, dX_o))
+        dX_exact_max = float(np.abs(o["X"] - x0).max())
+        Xo = storage_round(o["X"], dt)
+        del o
+        out["X"] = max(out["X"], rel(Xg - x0, Xo - x0))
         if dt == torch.bfloat16:
-            # X itself: within one bf16 unit in the last place of the larger of
-            # the two roundings, plus the tolerated error of the update itself
-            # (which decides the rounding where X' is near a rounding boundary).
-            mag = np.maximum(np.maximum(np.abs(Xo), np.abs(Xg)), 1e-30)
-            ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
-            slack = TOL[dt] * np.abs(o["X"] - host["X"][k]).max()
-            out["x_ulps"] = max(out["x_ulps"], float(np.max(np.abs(Xg - Xo) / (ulp + slack))))
+            out["x_ulps"] = max(out["x_ulps"], max_ulps(Xg, Xo, TOL[dt] * dX_exact_max))
+        del Xg, Xo
     out["status"] = status
     return out
 
 
-def muon_pair(G, M, X, head_dim, steps, coeff, mu, lr, wd, samples=None):
+def max_ulps(Xg, Xo, slack, rows=4096):
+    """max |Xg - Xo| / (ulp + slack) over all elements, in row blocks.  ulp is
+    one bfloat16 unit in the last place of the larger of the two stored
+    values; slack is the tolerated error of the unrounded update (the
+    relative tolerance times the largest update entry): two fp32 values that
+    differ by d round to bf16 values at most d plus one unit apart."""
+    worst = 0.0
+    for i in range(0, Xg.shape[0], rows):
+        g, o = Xg[i:i + rows], Xo[i:i + rows]
+        mag = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
+        ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+        worst = max(worst, float(np.max(np.abs(g - o) / (ulp + slack))))
+    return worst
+
+
+def muon_pair(G, M, X, head_dim, steps, coeff, mu, lr, wd, samples=None, form=oracle):
+    """One GPU Newton-Schulz step on the whole megabatch and the oracle (`form`)
+    on the sampled matrices; worst relative errors of O, M and the change of X."""
     batch, m, n = G.shape
     dt = G.dtype
     idx = list(range(batch)) if samples is None else list(samples)
@@ -86,7 +124,7 @@ def muon_pair(G, M, X, head_dim, steps, coeff, mu, lr, wd, samples=None):
     torch.cuda.synchronize()
     out = {"O": 0.0, "M": 0.0, "X": 0.0}
     for k, b in enumerate(idx):
-        o = oracle.muon_step(None if hX is None else hX[k], hG[k], None if hM is None else hM[k],
+        o = form.muon_step(None if hX is None else hX[k], hG[k], None if hM is None else hM[k],
                              head_dim=head_dim, steps=steps, coeff=coeff, mu=mu, lr=lr, wd=wd)
         out["O"] = max(out["O"], rel(f64(O[b]), o["O"]))
         if M is not None:

@@ -1,0 +1,38 @@
+"""Host-side logic of bench.py (CPU only): workload selection for profiling
+captures and the DRAM-traffic lookup from a committed ncu summary."""
+import bench
+import workloads as wl
+
+
+def test_select_groups_and_fraction():
+    w = bench.select_groups(wl.llama3_405b_layer(), [1, 3])
+    assert [(g.m, g.n) for g in w.groups] == [(16384, 1024), (53248, 16384)]
+    assert w.name == "llama3-405b-layer[1,3]"
+    w = bench.select_groups(wl.square(4096), None, 1.0 / 16)
+    assert w.groups[0].rank(w.fraction) == 256
+    assert bench.select_groups(wl.gpt_small(), None) == wl.gpt_small()
+
+
+def test_profiled_traffic_reads_summary_and_checks_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "dram_traffic_demo.txt").write_text(
+        "# ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum ...\n"
+        "csrc_sha256 abc123\n"
+        "launch 0 dion_update_tc read_bytes 100 write_bytes 50\n"
+        "launch 1 dion_update_tc read_bytes 300 write_bytes 150\n"
+        "launch 2 other_kernel read_bytes 7 write_bytes 7\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "csrc_digest", lambda: "abc123")
+    v, src = bench.profiled_traffic("demo", "dion_update_tc")
+    assert v == 300.0 and "2 launches" in src
+    assert bench.profiled_traffic("demo", "missing")[0] is None
+    assert bench.profiled_traffic("nothere", "dion_update_tc")[0] is None
+    monkeypatch.setattr(bench, "csrc_digest", lambda: "0" * 64)   # sources changed since the capture
+    v, why = bench.profiled_traffic("demo", "dion_update_tc")
+    assert v is None and "changed" in why
+
+
+def test_csrc_digest_covers_the_sources():
+    d = bench.csrc_digest()
+    assert len(d) == 64 and d == bench.csrc_digest()

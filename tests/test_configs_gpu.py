@@ -7,6 +7,7 @@ columns:
 
   P^T P = I                                   (orthonormal P)
   ||Q'_j|| = 1                                (unit-norm columns of the new Q)
+  Q'_j = R_j / ||R_j||                        (the new Q is R column-normalized)
   R[j, :] = sum_i B[i, j] P[i, :]             (R = B^T P, sampled columns j)
   M'[i, :] = B[i, :] - (1 - mu) P[i, :] R^T   (error feedback, sampled rows i)
   (B Q)[i, :] = P[i, :] (R^T Q)               (B Q lies in span(P); P^T B Q = R^T Q)
@@ -14,6 +15,7 @@ columns:
 
 plus, for Newton-Schulz, that O G^T is symmetric (k steps of the iteration act
 on singular values only: O = U p_k(S) V^T, so O G^T = U p_k(S) S U^T).
+The same shapes are compared with the oracle itself in test_full_size_gpu.py.
 """
 import math
 
@@ -58,6 +60,7 @@ def _check_dion_tensors(g, r, dtype, X, G, M, Q, mu, lr, wd, seed, bi):
     out = {}
     out["orth"] = float((P.T @ P - torch.eye(r, device=DEV, dtype=torch.float64)).abs().max())
     out["qnorm"] = float((Q[bi].double().norm(dim=0) - 1).abs().max())
+    out["qcol"] = float((Q[bi].double() - R / R.norm(dim=0).clamp_min(1e-30)).abs().max())
     cols = _sample(g.n, 64, seed + 1)
     rows = _sample(g.m, 64, seed + 2)
     out["R"] = _rel(R[cols], B[:, cols].T @ P)
@@ -77,6 +80,7 @@ def _check_dion_tensors(g, r, dtype, X, G, M, Q, mu, lr, wd, seed, bi):
 def _assert_dion(out, dtype):
     assert out["orth"] <= 1e-3, out
     assert out["qnorm"] <= 1e-4, out
+    assert out["qcol"] <= 1e-5, out
     for k in ("R", "M", "span"):
         assert out[k] <= TOL, (k, out)
     if dtype == torch.bfloat16:

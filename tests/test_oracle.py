@@ -284,3 +284,19 @@ def test_forms_agree_on_muon_step(hd):
     b = oracle.dense.muon_step(X, G, M, head_dim=hd, steps=5, mu=0.9, lr=0.1, wd=0.1)
     for key in ("O", "X", "M"):
         np.testing.assert_allclose(a[key], b[key], atol=1e-11, err_msg=key)
+
+
+@pytest.mark.parametrize("m,n", [(6, 9), (9, 6), (8, 8), (1, 5), (5, 1)])
+@pytest.mark.parametrize("steps", [1, 3, 5])
+def test_newton_schulz_rows_closed_form(m, n, steps):
+    """Sampled rows of Newton-Schulz through the step recursion equal the
+    same rows of U p_k(S / (||Y||_F + eps)) V^T from the exact SVD."""
+    rng = np.random.default_rng(m * 7 + n + 3 * steps)
+    Y = _rand(rng, m, n)
+    rows = np.arange(m)[::2] if m > 1 else np.array([0])
+    got = oracle.dense.newton_schulz_rows(Y, rows, steps, oracle.QUINTIC, oracle.NS_EPS)
+    want = _ns_closed_form(Y, steps, oracle.QUINTIC, oracle.NS_EPS)[rows]
+    np.testing.assert_allclose(got, want, atol=1e-12)
+    # and with the cubic coefficients (a different polynomial: pins the coefficient order)
+    got = oracle.dense.newton_schulz_rows(Y, rows, steps, oracle.CUBIC, oracle.NS_EPS)
+    np.testing.assert_allclose(got, _ns_closed_form(Y, steps, oracle.CUBIC, oracle.NS_EPS)[rows], atol=1e-12)
