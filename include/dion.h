@@ -34,13 +34,13 @@
  *   - Argument errors (shape, null pointer, alignment, dtype, workspace too
  *     small) are detected on the host and returned before anything is
  *     enqueued.  A failed kernel launch returns DION_ERR_CUDA.
- *   - Numeric breakdown found on the device (a Cholesky pivot in the
- *     orthonormalization of P at most 1e-6 times its column's squared norm,
- *     i.e. P is rank deficient to that tolerance, or a non-finite value)
- *     does not trap: it is recorded in a status word inside the
- *     workspace, read with dion_get_status after the caller has synchronized
- *     the stream.  Columns of P found dependent are set to zero, so the step
- *     still completes with finite output at a lower rank.
+ *   - Numeric events found on the device do not trap: they are recorded in a
+ *     status word inside the workspace, read with dion_get_status after the
+ *     caller has synchronized the stream (bits listed there).  A column of
+ *     P whose part outside the span of the columns before it is below 1e-6
+ *     of its norm (P rank deficient to that tolerance, decided in float64)
+ *     is set to zero, so the step still completes with finite output at a
+ *     lower rank.
  *   - Calls are not thread-safe with respect to one workspace: two calls in
  *     flight at once must use different workspaces.
  */
@@ -88,7 +88,13 @@ dion_status dion_workspace_size(int batch, int m, int n, int r, dion_dtype dt, s
  *                            256-byte aligned; its contents need not be
  *                            initialized and are scratch after the call
  *                            (except the status word, see dion_get_status)
- * P is orthonormalized by CholeskyQR2 in float32.
+ * P is orthonormalized by CholeskyQR2 in float32.  Matrices whose first
+ * float32 pass meets a pivot below 1e-6 of its column's squared norm (a
+ * dominant direction: P's condition number beyond about 1e3, or true rank
+ * deficiency) redo that first pass in float64 from the same panel, which
+ * resolves condition numbers up to about 1e7; the other matrices of the
+ * batch are not affected.  That fallback costs O(r^3) float64 work on one SM
+ * per flagged matrix (about 0.1 s at r = 1024).
  */
 dion_status dion_step_batched(int batch, int m, int n, int r, dion_dtype dt,
                               void* X, const void* G, float* M, float* Q,
@@ -145,9 +151,11 @@ dion_status dion_step_batched_dev(int batch, int m, int n, int r, dion_dtype dt,
  *     contents (the step clears what must start at zero itself).  Calls that
  *     overlap on the GPU (on different streams, or from different threads)
  *     race on it and give wrong results: serialize them.
- *   - The status word is not readable by the caller for this variant; a
- *     numeric breakdown still yields finite output (dependent columns of P
- *     are zeroed) as for dion_step_batched.
+ *   - The status word is not readable by the caller for this variant: a
+ *     rank-deficient P still yields finite output (dependent columns of P
+ *     are zeroed) as for dion_step_batched, but a kernel that gave up
+ *     waiting (status bit 4 of dion_get_status, outputs undefined) is not
+ *     reported either; the call still returns DION_OK.
  */
 dion_status dion_step_batched_static(int batch, int m, int n, int r, dion_dtype dt,
                                      void* X, const void* G, float* M, float* Q,
@@ -202,9 +210,16 @@ dion_status muon_ns_batched(int batch, int m, int n, int head_dim, dion_dtype dt
  * Reads the device status word of a workspace used by dion_step_batched or
  * muon_ns_batched (a blocking device-to-host copy of 4 bytes; synchronize
  * the stream of the last call first).  *device_status = 0 means no numeric
- * breakdown; otherwise a bit set: 1 = a Cholesky pivot at most 1e-6 times
- * its column's squared norm (rank-deficient P), 2 = non-finite value met.  The word is cleared at the start
- * of every step.  Returns DION_ERR_NUMERIC when the word is non-zero.
+ * event; otherwise bits are set:
+ *   1  a column of P was found dependent (its part outside the span of the
+ *      columns before it is below 1e-6 of its norm): P is rank deficient,
+ *      the column was set to zero, the step is valid at the lower rank;
+ *   2  a non-finite value was met (input, hyper-parameter or pivot);
+ *   4  a pipelined tensor-core kernel gave up waiting on one of its own
+ *      internal barriers (after 2 s; a correct run never gets there) and
+ *      stopped early: the outputs of that step (X, M, Q) are undefined.
+ * The word is cleared at the start of every step.  Returns DION_ERR_NUMERIC
+ * when the word is non-zero.
  */
 dion_status dion_get_status(const void* workspace, int* device_status);
 

@@ -14,10 +14,11 @@ static size_t carve(size_t& off, size_t bytes)
 }
 
 // Splits of a streaming contraction so that one wave of CTAs covers the SMs
-// (one CTA per SM); fixed per shape so that the workspace size is too.
+// (one CTA per SM) of the current device; fixed per shape and device, so
+// that the workspace size is too.
 static int stream_splits(long long base_ctas, int kchunks)
 {
-    const int sms = 152;
+    const int sms = num_sms();
     int s = (int)((sms + base_ctas / 2) / base_ctas);
     if (s < 1) s = 1;
     if (s > kchunks) s = kchunks;
@@ -42,6 +43,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
     L.W = carve(off, b * r * r * f);
     L.dead = carve(off, b * r * sizeof(int));
     L.inv = carve(off, b * rp * f);
+    L.hard = carve(off, (b + 1) * sizeof(int));
     if (L.tc) {
         const int rch = (int)cdiv(L.rp, 256);
         // wider than one 256-column chunk: B = M + G is formed once in bf16
@@ -67,9 +69,14 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
             L.B16 = carve(off, b * m * np * h);
             L.B16T = carve(off, b * n * mp * h);
             L.P16T = carve(off, b * rp * mp * h);
+        } else if (n % 8 == 0) {   // the B Q pass stores B = M + G in bf16 for the B^T P GEMM
+            L.b16_narrow = true;
+            L.B16 = carve(off, b * m * (size_t)n * h);
+            L.B16T = L.P16T = off;
         } else {
             L.B16 = L.B16T = L.P16T = off;
         }
+        L.S64 = L.S6;   // 6 b r r floats hold the 2 b r r doubles of the float64 first pass
         L.nbc = chol_block_size(r);
         if (L.nbc > 0) {
             const size_t nb = (size_t)L.nbc;
@@ -84,6 +91,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.ZJ = L.A3 = L.B16 = L.B16T = L.P16T = off;
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
         L.P3 = L.P3b = L.Z3 = L.S6 = L.normp = L.rcount = L.emax = off;
+        L.S64 = carve(off, 2 * b * r * r * sizeof(double));
     }
     L.total = off;
     return L;

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <atomic>
 #include <utility>
 
 #include "../../include/dion.h"
@@ -69,6 +70,22 @@ cudaError_t launch(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 b
     kernel<<<grid, block, smem, s>>>(std::forward<Args>(args)...);
     cudaError_t e = cudaGetLastError();
     prof_end(slot, s);
+    return e;
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device (the attribute is per device).  `done` is a bit mask of devices
+// already set up; concurrent first calls may both set the attribute, which is
+// harmless.  Devices beyond 63 are set up on every call.
+inline cudaError_t smem_attr_once(const void* func, int bytes, std::atomic<unsigned long long>& done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 

@@ -108,6 +108,7 @@ struct PassArgs {
     const bf16* G;
     float* part;            // [split][batch][rows][rp] fp32 partial products
     int* status;
+    bool store_b;           // B Q pass only: also store B = M + G, as rounded for the MMA, through tmS
 };
 
 constexpr int kProducers = 512;                  // warps 0..15 build the B tiles
@@ -133,7 +134,9 @@ constexpr size_t kPassSmem = (size_t)kStages * kStage + 1024 + 256;
 // buffered in tensor memory, so the epilogue warps write the fp32 partials of
 // one unit while the next unit streams.
 template <bool MN_A, bool VEC>
-__global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB, PassArgs a)
+__global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __grid_constant__ CUtensorMap tmB,
+                                                                       const __grid_constant__ CUtensorMap tmS,
+                                                                       PassArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -267,12 +270,21 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
                         const uint64_t bd = tc::make_sdesc(b0 + k * 2048, 8192, 1024);
                         tc::mma_bf16(d, ad, bd, idesc, (kc | k) != 0);
                     }
+                    if (!MN_A && a.store_b) {
+                        // the bf16 B tile (128 rows x 64 columns, 128-byte swizzled as the
+                        // tensor map expects) to global memory for the B^T P GEMM; the
+                        // stage is released only after the store has read it
+                        tc::tma_store_3d(&tmS, smem + stage * kStage, (kc0 + kc) * kBK, tile * kBM, b);
+                        tc::tma_store_commit();
+                        tc::tma_store_wait_read();
+                    }
                     tc::mma_commit(&empty[stage]);
                     if (++stage == kStages) { stage = 0; ph ^= 1; }
                 }
                 if (!ok) break;
                 tc::mma_commit(&acc_full[buf]);
             }
+            if (!MN_A && a.store_b) tc::tma_store_wait_all();
         }
     } else {
         // ---------------- epilogue: TMEM -> fp32 partials
@@ -456,6 +468,12 @@ struct UpdPArgs {
     int m, n, batch, kchunks, tiles_m, tiles_n;
     StepHyper hp;
     int* status;
+    // tile order within a matrix: m_fast walks the row tiles fastest (the P
+    // panel cycles, each R/Q chunk is used by consecutive tiles), else the
+    // column tiles (R/Q cycle, each P chunk is used by consecutive tiles).
+    // The shorter direction goes fastest, so the operands that cycle stay a
+    // few MB and remain in L2 while M, G and X stream through it.
+    int m_fast;
 };
 
 constexpr uint32_t kPStage = kUStage;                              // 32 KB of operands per K chunk
@@ -525,7 +543,8 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
             int it = 0;
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
                 const int b = t / per_mat, rem = t % per_mat;
-                const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
+                const int m0 = (a.m_fast ? rem % a.tiles_m : rem / a.tiles_n) * kBM;
+                const int n0 = (a.m_fast ? rem / a.tiles_m : rem % a.tiles_n) * kUBN;
                 const int eb = it % EPI;
                 if (!tc::mbar_wait(&eempty[eb], ((it / EPI) & 1) ^ 1, abrt, a.status)) break;
                 uint8_t* e = epi + eb * kEBuf;
@@ -579,7 +598,8 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
         int it = 0;
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
             const int b = t / per_mat, rem = t % per_mat;
-            const int m0 = (rem / a.tiles_n) * kBM, n0 = (rem % a.tiles_n) * kUBN;
+            const int m0 = (a.m_fast ? rem % a.tiles_m : rem / a.tiles_n) * kBM;
+            const int n0 = (a.m_fast ? rem / a.tiles_m : rem % a.tiles_n) * kUBN;
             const int ab = it & 1, eb = it % EPI;
             const uint32_t aph = (it >> 1) & 1, eph = (it / EPI) & 1;
             const bool ok = tc::mbar_wait(&afull[ab], aph, abrt, a.status) &&
@@ -905,19 +925,17 @@ static unsigned grid_for(long long work, int per = 256 * 4)
 }
 
 template <bool MN_A>
-static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm, const PassArgs& pa, cudaStream_t st)
+static cudaError_t launch_pass(const char* name, bool vec, const CUtensorMap& tm, const CUtensorMap& tms,
+                               const PassArgs& pa, cudaStream_t st)
 {
     const int out_rows = MN_A ? pa.n : pa.m;
     const long long units = cdiv(out_rows, kBM) * (long long)pa.splits * pa.batch;
     const dim3 grid((unsigned)std::min<long long>(units, num_sms()));
-    static bool attr[2] = {false, false};
+    static std::atomic<unsigned long long> attr[2] = {{0}, {0}};
     auto k = vec ? dion_pass_kernel<MN_A, true> : dion_pass_kernel<MN_A, false>;
-    if (!attr[vec]) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPassSmem);
-        if (e != cudaSuccess) return e;
-        attr[vec] = true;
-    }
-    return launch(name, k, grid, dim3(kPassWarps * 32), kPassSmem, st, tm, pa);
+    cudaError_t e = smem_attr_once((const void*)k, (int)kPassSmem, attr[vec]);
+    if (e != cudaSuccess) return e;
+    return launch(name, k, grid, dim3(kPassWarps * 32), kPassSmem, st, tm, tms, pa);
 }
 
 dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* Gv, float* M, float* Q, float mu,
@@ -970,7 +988,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         e.Cf = part; e.ldc = rp; e.sc = (long long)m * rp; e.alpha = 0.f; e.beta = 1.f; e.status = status;
         e.nseg = 1; e.zmul = 1;
         DION_TRY(tc_gemm<256>("dion_bq_tc", tA, tB, n, e, st));
-        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, 1, P0, P1, P16, ws, L, status, st));
+        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, 1, P0, P1, P16, ws, L, status, st, n, M, G, Q));
         // 6'. R = B^T P: A = B^T (n x m), B = P^T (rp x m), both K-major
         bf16* P16T = (bf16*)(ws + L.P16T);
         DION_TRY(launch("dion_transpose_p", dion_transpose16_kernel,
@@ -987,32 +1005,57 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
                         batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
     } else {
-    // 2. P partials = B Q
+    // 2. P partials = B Q (with n % 8 == 0 the pass also stores B in bf16)
     CUtensorMap tmQt;
     if (!make_tmap_3d(&tmQt, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 64))
+        return DION_ERR_CUDA;
+    bf16* B16 = L.b16_narrow ? (bf16*)(ws + L.B16) : nullptr;
+    CUtensorMap tmS = tmQt;   // where the B Q pass stores bf16 B (unused without B16)
+    if (B16 && !make_tmap_3d(&tmS, B16, TmapType::BF16, n, m, batch, (long long)n * 2, (long long)m * n * 2, 64, kBM))
         return DION_ERR_CUDA;
     {
         const int kchunks = (int)cdiv(n, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status};
-        DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, pa, st));
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, B16 != nullptr};
+        DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, tmS, pa, st));
         // 3-5. CholeskyQR2; its first pass reads the split partials of P directly, its
         // last product writes P (float32, P0) and P16 = bf16(P)
-        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st));
+        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st, n, M, G, Q));
     }
     // 6. R partials = B^T P
-    CUtensorMap tmP64;
-    if (!make_tmap_3d(&tmP64, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
-        return DION_ERR_CUDA;
-    {
+    const int nchunks = (int)cdiv(n, kRChunk);
+    if (B16) {
+        // as a TMA GEMM on the stored bf16 B: A = B^T read MN-major from the
+        // row-major B (64 x 64 boxes), B operand = P16 read MN-major; one split
+        CUtensorMap tA, tB;
+        const int bn = rp <= 64 ? 64 : (rp <= 128 ? 128 : (rp <= 192 ? 192 : 256));
+        if (!make_tmap_3d(&tA, B16, TmapType::BF16, n, m, batch, (long long)n * 2, (long long)m * n * 2, 64, 64) ||
+            !make_tmap_3d(&tB, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
+            return DION_ERR_CUDA;
+        TcGemmEpi e{};
+        e.M = n; e.N = rp; e.tiles_m = (int)cdiv(n, kBM); e.tiles_n = (int)cdiv(rp, bn); e.batch = batch;
+        e.Cf = part; e.ldc = rp; e.sc = (long long)n * rp; e.alpha = 0.f; e.beta = 1.f; e.status = status;
+        e.nseg = 1; e.zmul = 1;
+        cudaError_t ce;
+        if (bn == 64) ce = tc_gemm<64, true>("dion_btp_tc", tA, tB, m, e, st);
+        else if (bn == 128) ce = tc_gemm<128, true>("dion_btp_tc", tA, tB, m, e, st);
+        else if (bn == 192) ce = tc_gemm<192, true>("dion_btp_tc", tA, tB, m, e, st);
+        else ce = tc_gemm<256, true>("dion_btp_tc", tA, tB, m, e, st);
+        DION_TRY(ce);
+        // 7. R = the one partial, R16, column norms, Q = R / ||R_j||, Q16
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
+                        batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
+    } else {
+        CUtensorMap tmP64;
+        if (!make_tmap_3d(&tmP64, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
+            return DION_ERR_CUDA;
         const int kchunks = (int)cdiv(m, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit_r);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status};
-        DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, pa, st));
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, false};
+        DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, tmP64, pa, st));
         // 7. R = sum of partials, R16, column norms, Q = R / ||R_j||, Q16
-        const int nchunks = (int)cdiv(n, kRChunk);
         DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp,
                         splits, batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
     }
@@ -1045,12 +1088,14 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         e1.auxf = M; e1.ldauxf = n; e1.sauxf = mn; e1.alpha = 1.f;
         e1.aux2 = G; e1.ldaux2 = n; e1.saux2 = mn; e1.alpha2 = 1.f;
         e1.hp = hp; e1.hp_mode = 1; e1.status = status; e1.nseg = 1; e1.zmul = 1;
+        e1.m_fast = e1.tiles_m < e1.tiles_n;
         DION_TRY(tc_gemm<256>("dion_update_tc", tP, tRb, rp, e1, st));
         TcGemmEpi e2{};
         e2.M = m; e2.N = n; e2.tiles_m = e1.tiles_m; e2.tiles_n = e1.tiles_n; e2.batch = batch;
         e2.C = X; e2.ldc = n; e2.sc = mn;
         e2.aux = X; e2.ldaux = n; e2.saux = mn;
         e2.hp = hp; e2.hp_mode = 2; e2.status = status; e2.nseg = 1; e2.zmul = 1;
+        e2.m_fast = e2.tiles_m < e2.tiles_n;
         DION_TRY(tc_gemm<256>("dion_update_tc", tP, tQb, rp, e2, st));
     } else if (vec) {
         // persistent TMA-epilogue pass (needs 16-byte aligned rows of M, G, X)
@@ -1063,33 +1108,22 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int tm = (int)cdiv(m, kBM), tn = (int)cdiv(n, kUBN);
         const long long tiles = (long long)tm * tn * batch;
         const int grid = (int)std::min<long long>(tiles, num_sms());
-        UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, hp, status};
+        UpdPArgs ua{m, n, batch, (int)cdiv(rp, kBK), tm, tn, hp, status, tm < tn ? 1 : 0};
         if (ua.kchunks <= 4) {
-            static bool pattr = false;
-            if (!pattr) {
-                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<3, 2>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<3, 2>()));
-                pattr = true;
-            }
+            static std::atomic<unsigned long long> pattr{0};
+            DION_TRY(smem_attr_once((const void*)dion_update_persist_kernel<3, 2>, (int)upd_smem<3, 2>(), pattr));
             DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<3, 2>, dim3(grid), dim3(192), upd_smem<3, 2>(),
                             st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
         } else {
-            static bool pattr_w = false;
-            if (!pattr_w) {
-                DION_TRY(cudaFuncSetAttribute(dion_update_persist_kernel<5, 1>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem<5, 1>()));
-                pattr_w = true;
-            }
+            static std::atomic<unsigned long long> pattr_w{0};
+            DION_TRY(smem_attr_once((const void*)dion_update_persist_kernel<5, 1>, (int)upd_smem<5, 1>(), pattr_w));
             DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<5, 1>, dim3(grid), dim3(192), upd_smem<5, 1>(),
                             st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
         }
     } else {
-        static bool attr[2] = {false, false};
+        static std::atomic<unsigned long long> attr[2] = {{0}, {0}};
         auto k = vec ? dion_update_tc_kernel<true> : dion_update_tc_kernel<false>;
-        if (!attr[vec]) {
-            DION_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUpdSmem));
-            attr[vec] = true;
-        }
+        DION_TRY(smem_attr_once((const void*)k, (int)kUpdSmem, attr[vec]));
         UpdArgs ua{m, n, rp, (int)cdiv(rp, kBK), M, G, X, hp, status};
         DION_TRY(launch("dion_update_tc", k, dim3((unsigned)cdiv(n, kUBN), (unsigned)cdiv(m, kBM), batch), dim3(192),
                         kUpdSmem, st, tmPa, tmR, tmQ, ua));

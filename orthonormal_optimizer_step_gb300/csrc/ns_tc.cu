@@ -18,16 +18,20 @@
 
 namespace dion {
 
+// SM count of the current device, cached per device (thread-safe: a race
+// only repeats the query).
 int num_sms()
 {
-    static int dev = -1, n = 0;
+    static std::atomic<int> cache[64];
     int cur = 0;
-    cudaGetDevice(&cur);
-    if (cur != dev || n == 0) {
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, cur);
-        dev = cur;
-        if (n <= 0) n = 1;
+    if (cudaGetDevice(&cur) != cudaSuccess) cur = 0;
+    if (cur >= 0 && cur < 64) {
+        const int c = cache[cur].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, cur) != cudaSuccess || n <= 0) n = 1;
+    if (cur >= 0 && cur < 64) cache[cur].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -146,6 +150,12 @@ __global__ void __launch_bounds__(256) ns_finish_tr_kernel(int m, int n, int hd,
     }
 }
 
+// Row-tile bands of the Newton-Schulz GEMMs (see TcGemmEpi::band_m): with
+// 152 CTAs in flight, 16 row tiles by about 9 column tiles of 256 share their
+// operand panels in L2 (about 4.5k panel rows against 17k for a whole row of
+// column tiles).
+constexpr int kNsBand = 16;
+
 static int pick_bn(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 
 static cudaError_t gemm_bn_mn(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K,
@@ -217,14 +227,17 @@ dion_status muon_tc(int batch, int m, int n, dion_dtype dt, void* X, const void*
         if (!ok) return DION_ERR_CUDA;
         // A = Y Y^T
         TcGemmEpi e1{s, s, tm, (int)cdiv(s, bn_s), nb, A, sp, sa, nullptr, 0, 0, nullptr, 0, 0, 0.f, 1.f, status, nullptr, 1, 1, 0, 0u, 0u};
+        e1.band_m = kNsBand;
         DION_TRY(gemm_bn(bn_s, "ns_gram_tc", tYa_a, tYa_b, l, e1, st));
         // Bm = b A + c A A   (A symmetric: A A = A A^T)
         TcGemmEpi e2{s, s, tm, (int)cdiv(s, bn_s), nb, Bm, sp, sa, A, sp, sa, nullptr, 0, 0, coeff[1], coeff[2],
                      status, nullptr, 1, 1, 0, 0u, 0u};
+        e2.band_m = kNsBand;
         DION_TRY(gemm_bn(bn_s, "ns_poly_tc", tA_a, tA_b, s, e2, st));
         // Y' = a Y + Bm Y: both operands MN-major (Bm symmetric, Y row-major with K = s rows)
         TcGemmEpi e3{s, l, tm, (int)cdiv(l, bn_l), nb, Yb, lp, sy, Ya, lp, sy, nullptr, 0, 0, coeff[0], 1.f, status,
                      nullptr, 1, 1, 0, 0u, 0u};
+        e3.band_m = kNsBand;
         DION_TRY(gemm_bn_mn(bn_l, "ns_axpy_tc", tBm_mn, tYa_mn, s, e3, st));
         std::swap(Ya, Yb);
     }

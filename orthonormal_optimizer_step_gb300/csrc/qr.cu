@@ -307,7 +307,10 @@ __global__ void __launch_bounds__(512, 1) chol_inv_kernel(int r, const float* Si
     }
 #undef Lx0
 #undef Lx
-    if (tid == 0 && s_bad) atomicOr(status, s_bad);
+    if (tid == 0 && s_bad) {
+        atomicOr(status + (size_t)b * in.sstride, s_bad);
+        if (in.any) atomicOr(in.any, 1);
+    }
 }
 
 // ---- Register-resident inverse Cholesky for r <= kGjMaxR, one CTA per matrix.
@@ -750,7 +753,10 @@ __global__ void __launch_bounds__(512, 1) chol_gj_kernel(int r, const float* Sin
         __syncthreads();
     }
     __syncthreads();
-    if (tid == 0 && s_bad) atomicOr(status, s_bad);
+    if (tid == 0 && s_bad) {
+        atomicOr(status + (size_t)b * in.sstride, s_bad);
+        if (in.any) atomicOr(in.any, 1);
+    }
 }
 
 static size_t chol_smem_bytes(int r, bool in_smem)
@@ -760,11 +766,11 @@ static size_t chol_smem_bytes(int r, bool in_smem)
 }
 
 cudaError_t chol_inv(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf, float* W, bf16* Z3,
-                     int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre)
+                     int ldz, int* dead, int* status, cudaStream_t st, const int* emax_pre, long long sstride, int* any)
 {
     const long long rr = (long long)r * r;
     return chol_inv_io(name, batch, r, Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status, st, emax_pre,
-                       CholIn{nparts * rr, rr, r, r});
+                       CholIn{nparts * rr, rr, r, r, nullptr, 0, sstride, any});
 }
 
 cudaError_t chol_inv_io(const char* name, int batch, int r, const float* Sin, int nparts, float* Swork, float* Wbuf,
@@ -774,33 +780,34 @@ cudaError_t chol_inv_io(const char* name, int batch, int r, const float* Sin, in
     if (in.lds == 0 && (r > kGjMaxR || nparts != 1)) return cudaErrorInvalidValue;   // block-major input
     if (r <= kGjMaxR) {
         if (nparts < 1 || nparts > kGjMaxParts) return cudaErrorInvalidValue;
-        static bool gj_attr = false;
+        static std::atomic<unsigned long long> gj_attr{0};
         const size_t smem = (size_t)kGjStageRows * (align_up((size_t)r, 8) + 4) * sizeof(float);
-        if (!gj_attr) {
-            cudaError_t e = cudaFuncSetAttribute(chol_gj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)((size_t)kGjStageRows * (kGjMaxR + 4) * sizeof(float)));
-            if (e != cudaSuccess) return e;
-            gj_attr = true;
-        }
+        cudaError_t e = smem_attr_once((const void*)chol_gj_kernel,
+                                       (int)((size_t)kGjStageRows * (kGjMaxR + 4) * sizeof(float)), gj_attr);
+        if (e != cudaSuccess) return e;
         return launch(name, chol_gj_kernel, dim3(batch), dim3(512), smem, st, r, Sin, nparts, W, Z3, ldz, dead, status,
                       emax_pre, in);
     }
-    static bool gattr = false;
-    if (!gattr) {   // 3 r floats of dynamic shared memory: up to 48 KB at r = 4096, plus the static part
-        cudaError_t e = cudaFuncSetAttribute(chol_inv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             96 * 1024);
-        if (e != cudaSuccess) return e;
-        gattr = true;
-    }
+    // 3 r floats of dynamic shared memory: up to 48 KB at r = 4096, plus the static part
+    static std::atomic<unsigned long long> gattr{0};
+    cudaError_t e = smem_attr_once((const void*)chol_inv_kernel<false>, 96 * 1024, gattr);
+    if (e != cudaSuccess) return e;
     if (chol_smem_bytes(r, false) > 96 * 1024) return cudaErrorInvalidValue;
     return launch(name, chol_inv_kernel<false>, dim3(batch), dim3(512), chol_smem_bytes(r, false), st, r,
                   Sin, nparts, Swork, Wbuf, W, Z3, ldz, dead, status, emax_pre, in);
 }
 
 cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float* Ptmp, float* S, float* W,
-                         int* dead, int* status, cudaStream_t st)
+                         int* dead, int* status, int* hard, double* S64, cudaStream_t st)
 {
     const long long sp = (long long)m * ldp, ss = (long long)r * r;
+    // the first pass reports unresolved pivots per matrix (hard); those
+    // matrices redo it in float64 (qr64.cu) before the second pass
+    const bool fb = qr64_supported(r) && ldp == r;
+    if (fb) {
+        cudaError_t e = cudaMemsetAsync(hard, 0, sizeof(int) * (batch + 1), st);
+        if (e != cudaSuccess) return e;
+    }
     float* src = P;
     float* dst = Ptmp;
     for (int pass = 0; pass < 2; ++pass) {
@@ -808,13 +815,18 @@ cudaError_t qr_cholesky2(int batch, int m, int r, long long ldp, float* P, float
                                      LdB<float, true>{src, sp, ldp}, LdB<float, true>{src, sp, ldp},
                                      EpStore{S, ss, r}, st);
         if (e != cudaSuccess) return e;
+        const bool first_fb = fb && pass == 0;
         e = chol_inv(pass == 0 ? "chol_inv_pass1" : "chol_inv_pass2", batch, r, S, 1, S, W, W, nullptr, 0, dead,
-                     status, st);
+                     first_fb ? hard : status, st, nullptr, first_fb ? 1 : 0, first_fb ? hard + batch : nullptr);
         if (e != cudaSuccess) return e;
         // P <- P L^{-T}: B(k, j) = L^{-1}[j][k]
         e = gemm_simt<1>("qr_apply", batch, m, r, r, LdA<float, true>{src, sp, ldp}, LdB<float, false>{W, ss, r},
                          LdB<float, false>{W, ss, r}, EpStore{dst, sp, ldp}, st);
         if (e != cudaSuccess) return e;
+        if (first_fb) {
+            e = qr64_first_pass(batch, m, r, r, P, 1, 0, S64, dst, nullptr, dead, status, hard, st);
+            if (e != cudaSuccess) return e;
+        }
         float* t = src; src = dst; dst = t;
     }
     return cudaSuccess;  // two passes: the result is back in P

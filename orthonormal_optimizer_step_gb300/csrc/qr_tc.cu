@@ -344,7 +344,8 @@ TcGemmEpi six_term_epi(int M, int N, int bn, int batch, int* status, const int* 
 // skipped by every kernel.
 cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const float* Psrc, float* dst, bf16* P16,
                                float* S, float* W, bf16* ZJ, bf16* A3, bf16* L3, bf16* P3, int* dead, int* status,
-                               const int* gate, bool keep_terms, cudaStream_t st)
+                               int* fac_status, long long fac_sstride, int* fac_any, const int* gate,
+                               bool keep_terms, cudaStream_t st)
 {
     const int nblk = (int)cdiv(r, nb);
     const long long z3 = 3ll * batch, rr = (long long)r * r, mrp = (long long)m * rp, rrp = (long long)r * rp;
@@ -358,7 +359,8 @@ cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const fl
         const int j0 = J * nb, w = std::min(nb, r - j0), rest = r - j0 - w;
         const int bnw = pick_bn_qr(w);
         cudaError_t e = chol_inv_io("chol_blk_diag", batch, w, S + (size_t)j0 * r + j0, 1, S, W, nullptr, ZJ, nb,
-                                    dead + j0, status, st, gate, CholIn{rr, 0, r, r, dg + j0, r});
+                                    dead + j0, fac_status, st, gate,
+                                    CholIn{rr, 0, r, r, dg + j0, r, fac_sstride, fac_any});
         if (e != cudaSuccess) return e;
         CUtensorMap tZ;
         if (!tmap_bf16(&tZ, ZJ, nb, w, z3, nb, (long long)w * nb, bnw)) return cudaErrorInvalidValue;
@@ -433,8 +435,9 @@ cudaError_t chol_blocked_apply(int batch, int m, int r, int rp, int nb, const fl
 
 int chol_block_size(int r) { return r > kCholOneCtaMaxR ? kCholBlock : 0; }
 
-cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, int nparts, float* P, float* Ptmp,
-                            bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st)
+cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* Pin, int nparts, float* P, float* Ptmp,
+                            bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st, int n,
+                            const float* M, const bf16* G, const float* Q)
 {
     bf16* P3 = (bf16*)(ws + L.P3);
     bf16* P3b = (bf16*)(ws + L.P3b);
@@ -444,6 +447,17 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
     float* W = (float*)(ws + L.W);
     int* dead = (int*)(ws + L.dead);
     int* emax = (int*)(ws + L.emax);
+    int* hard = (int*)(ws + L.hard);
+    // the first pass's factorization reports unresolved pivots per matrix
+    // (hard); those matrices redo the first pass in float64 (qr64.cu)
+    const bool fb = qr64_supported(r);
+    if (fb) {
+        cudaError_t e = cudaMemsetAsync(hard, 0, sizeof(int) * (batch + 1), st);
+        if (e != cudaSuccess) return e;
+    }
+    int* fac1 = fb ? hard : status;
+    int* any1 = fb ? hard + batch : nullptr;
+    const long long fac1_stride = fb ? 1 : 0;
     const int bn = pick_bn_qr(r), bna = pick_bn_qr(rp);
     const bool blocked = L.nbc > 0;
     // blocked: the Gram's lower half, accumulated straight into S when that
@@ -517,8 +531,8 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                            dim3((unsigned)std::min<long long>(cdiv(sblk / 4, 256), 1024), batch), dim3(256), 0, st, r, 6,
                            (const float*)S6, S, sblk);
                 if (e != cudaSuccess) return e;
-                e = chol_inv_io("chol_inv_pass1", batch, r, S, 1, S, W, nullptr, Z3, rp, dead, status, st, nullptr,
-                                CholIn{sblk, 0, 0, r});
+                e = chol_inv_io("chol_inv_pass1", batch, r, S, 1, S, W, nullptr, Z3, rp, dead, fac1, st, nullptr,
+                                CholIn{sblk, 0, 0, r, nullptr, 0, fac1_stride, any1});
             } else {
                 e = chol_inv("chol_inv_pass2", batch, r, S6, 6, S, W, nullptr, Z3, rp, dead, status, st, gate);
             }
@@ -547,7 +561,16 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, const float* Pin, i
                 if (e != cudaSuccess) return e;
             }
             e = chol_blocked_apply(batch, m, r, rp, L.nbc, pass == 0 ? dst : src, dst, pass == 1 ? P16 : nullptr, S, W,
-                                   (bf16*)(ws + L.ZJ), (bf16*)(ws + L.A3), Z3, P3, dead, status, gate, pass == 0, st);
+                                   (bf16*)(ws + L.ZJ), (bf16*)(ws + L.A3), Z3, P3, dead, status,
+                                   pass == 0 ? fac1 : status, pass == 0 ? fac1_stride : 0, pass == 0 ? any1 : nullptr,
+                                   gate, pass == 0, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (pass == 0 && fb) {
+            // flagged matrices: B Q and the first pass again in float64 from the step's inputs,
+            // written where the second pass reads its input (blocked: P3 and the float32 panel; else P3b)
+            e = qr64_first_pass(batch, m, r, rp, Pin, nparts, (long long)batch * m * rp, (double*)(ws + L.S64),
+                                blocked ? dst : nullptr, blocked ? P3 : P3b, dead, status, hard, st, n, M, G, Q);
             if (e != cudaSuccess) return e;
         }
     }

@@ -89,7 +89,8 @@ static dion_status dion_simt_t(int batch, int m, int n, int r, T* X, const T* G,
     DION_TRY((gemm_simt<1>("dion_bq_simt", batch, m, r, n, LdSum<float, T, true>{M, G, mn, n},
                            LdB<float, true>{Q, nr, r}, LdB<float, true>{Q, nr, r}, EpStore{P0, mr, r}, st)));
     // P <- orthonormalize(P)
-    DION_TRY(qr_cholesky2(batch, m, r, r, P0, P1, S, W, dead, status, st));
+    DION_TRY(qr_cholesky2(batch, m, r, r, P0, P1, S, W, dead, status, (int*)(ws + L.hard), (double*)(ws + L.S64),
+                          st));
     // R = B^T P
     DION_TRY((gemm_simt<1>("dion_btp_simt", batch, n, r, m, LdSum<float, T, false>{M, G, mn, n},
                            LdB<float, true>{P0, mr, r}, LdB<float, true>{P0, mr, r}, EpStore{R, nr, r}, st)));

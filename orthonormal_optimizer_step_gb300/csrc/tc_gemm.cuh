@@ -52,7 +52,33 @@ struct TcGemmEpi {
     // beta = -lr sqrt(m/n).  Non-finite device values set the status word.
     StepHyper hp;
     int hp_mode;
+    // tile order within a matrix: 0 walks the column tiles fastest, 1 the row
+    // tiles (pick the shorter direction, so the operand tiles that cycle stay
+    // small enough for L2 while the other operand is reused by consecutive tiles)
+    int m_fast;
+    // band_m > 0 (overrides m_fast): bands of band_m row tiles, row tiles
+    // fastest inside a band.  The CTAs in flight then cover a few row tiles
+    // by a few column tiles, so both operand panels they stream are shared in
+    // L2 (for long K, where no single panel order keeps one operand resident)
+    int band_m;
 };
+
+__device__ __forceinline__ void tc_tile_mn(const TcGemmEpi& ep, int rem, int& tm, int& tn)
+{
+    if (ep.band_m > 0) {
+        const int per_band = ep.band_m * ep.tiles_n;
+        const int band = rem / per_band, in = rem - band * per_band;
+        const int m0 = band * ep.band_m, bm = min(ep.band_m, ep.tiles_m - m0);
+        tm = m0 + in % bm;
+        tn = in / bm;
+    } else if (ep.m_fast) {
+        tm = rem % ep.tiles_m;
+        tn = rem / ep.tiles_m;
+    } else {
+        tm = rem / ep.tiles_n;
+        tn = rem % ep.tiles_n;
+    }
+}
 
 template <int BN>
 struct TcGemmCfg {
@@ -268,7 +294,8 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t ph = 0;
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
                 const int b = t / per_mat, rem = t % per_mat;
-                const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+                int tm, tn;
+                tc_tile_mn(ep, rem, tm, tn);
                 if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
                 const int q0 = ep.seg_batch ? b % ep.nseg : 0, q1 = ep.seg_batch ? q0 + 1 : ep.nseg;
                 const int bm = ep.seg_batch ? b / ep.nseg : b;
@@ -306,7 +333,9 @@ __global__ void __launch_bounds__(192, 1)
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
                 {
                     const int b = t / per_mat, rem = t % per_mat;
-                    if (!tc_tile_on(ep, b, rem / ep.tiles_n, rem % ep.tiles_n, Cfg::BM, BN)) continue;
+                    int tm, tn;
+                    tc_tile_mn(ep, rem, tm, tn);
+                    if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
                 }
                 const int buf = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
@@ -354,7 +383,8 @@ __global__ void __launch_bounds__(192, 1)
         int it = 0;
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
             const int b = t / per_mat, rem = t % per_mat;
-            const int tm = rem / ep.tiles_n, tn = rem % ep.tiles_n;
+            int tm, tn;
+            tc_tile_mn(ep, rem, tm, tn);
             if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
             const int buf = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -389,13 +419,9 @@ cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap&
                     cudaStream_t st)
 {
     using Cfg = TcGemmCfg<BN>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = smem_attr_once((const void*)tc_gemm_kernel<BN, MN>, (int)Cfg::SMEM, attr);
+    if (e != cudaSuccess) return e;
     const int tiles = ep.batch * ep.tiles_m * ep.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
     return launch(name, tc_gemm_kernel<BN, MN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
