@@ -463,7 +463,10 @@ __global__ void __launch_bounds__(192) dion_update_tc_kernel(const __grid_consta
 // of the next tile run under the math and the stores of this one), the P, R
 // and Q operands stream through two K stages, and the two accumulators
 // (P R^T, P Q^T) are double-buffered in tensor memory.
-//   warp 4: TMA producer     warp 5: MMA issuer     warps 0..3: epilogue
+//   warps 0..7: epilogue (warp w: TMEM lane quarter w % 4, 32-column half w / 4;
+//               two warps per scheduler, so the TMEM and shared-memory
+//               latencies of one overlap the arithmetic of the other)
+//   warp 8: TMA producer     warp 9: MMA issuer
 struct UpdPArgs {
     int m, n, batch, kchunks, tiles_m, tiles_n;
     StepHyper hp;
@@ -485,8 +488,11 @@ constexpr uint32_t kEBuf = kEM + kEG + kEX;                        // 64 KB
 template <int OPS, int EPI>
 constexpr size_t upd_smem() { return OPS * (size_t)kPStage + EPI * (size_t)kEBuf + 1024 + 256; }
 
+constexpr int kUpdEpiWarps = 8;
+constexpr int kUpdThreads = (kUpdEpiWarps + 2) * 32;
+
 template <int OPS, int EPI>
-__global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
+__global__ void __launch_bounds__(kUpdThreads, 1) dion_update_persist_kernel(
     const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmR,
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmM,
     const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX, UpdPArgs a)
@@ -522,12 +528,12 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&afull[s], 1);
-            tc::mbar_init(&aempty[s], 4);
+            tc::mbar_init(&aempty[s], kUpdEpiWarps);
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kUpdEpiWarps + 1) {
         tc::tmem_alloc(tmem_slot, 256);
         tc::tmem_relinquish();
     }
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kUpdEpiWarps) {
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kUpdEpiWarps + 1) {
         if (lane == 0) {
             const uint32_t idesc = tc::make_idesc(kBM, kUBN, 1, false, false);
             int stage = 0;
@@ -594,7 +600,8 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
             }
         }
     } else {
-        const int row = warp * 32 + lane;            // tile row == TMEM lane
+        const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter, 32-column half
+        const int row = quarter * 32 + lane;          // tile row == TMEM lane
         int it = 0;
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
             const int b = t / per_mat, rem = t % per_mat;
@@ -606,13 +613,12 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                             tc::mbar_wait(&efull[eb], eph, abrt, a.status);
             tc::tc_fence_after();
             uint8_t* e = epi + eb * kEBuf;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {            // 32-column halves
+            {
                 uint32_t pr[32], pq[32];
-                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ab * 128 + h * 32), pr);
-                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ab * 128 + kUBN + h * 32), pq);
+                tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * 128 + h * 32), pr);
+                tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * 128 + kUBN + h * 32), pq);
                 tc::tmem_ld_wait();
-                if (!ok) continue;
+                if (ok) {
                 uint8_t* eM = e + h * 16384;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {        // M: 8 chunks of 4 floats
@@ -637,12 +643,13 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
                         o[q] = decay * __bfloat162float(xh[q]) - scale * __uint_as_float(pq[8 * c + q]);
                     *px = pack8(o);
                 }
+                }
             }
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&aempty[ab]);
             tc::fence_proxy_async_smem();
-            tc::named_bar_sync(1, 128);
+            tc::named_bar_sync(1, kUpdEpiWarps * 32);
             if (threadIdx.x == 0) {
                 if (ok) {
                     tc::tma_store_3d(&tmM, e, n0, m0, b);
@@ -657,7 +664,7 @@ __global__ void __launch_bounds__(192, 1) dion_update_persist_kernel(
         if (threadIdx.x == 0) tc::tma_store_wait_all();
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kUpdEpiWarps + 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 256);
     }
@@ -803,6 +810,9 @@ constexpr int kRChunk = 32;
 // zeroed by dion_prep_qt_kernel earlier in the step) reduces the chunks in
 // order into inv[b][c] = 1 / max(||R_c||, floor) (0 for padding columns) and
 // resets the counter.
+// kCopy = false: the B^T P GEMM already wrote R and R16; part is R itself
+// (one partial) and only the column norms are formed.
+template <bool kCopy>
 __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, int splits, int batch,
                                                         const float* __restrict__ part, float* __restrict__ R,
                                                         bf16* __restrict__ R16, float* __restrict__ normpart,
@@ -844,8 +854,11 @@ __global__ void __launch_bounds__(256) dion_rsum_kernel(int n, int r, int rp, in
                 if (c + 2 >= r) x.z = 0.f;
                 if (c + 3 >= r) x.w = 0.f;
                 const long long o = ((long long)b * n + j) * rp + c;
-                *reinterpret_cast<float4*>(R + o) = x;
-                *reinterpret_cast<uint2*>(R16 + o) = make_uint2(tc::pack_bf16x2(x.x, x.y), tc::pack_bf16x2(x.z, x.w));
+                if (kCopy) {
+                    *reinterpret_cast<float4*>(R + o) = x;
+                    *reinterpret_cast<uint2*>(R16 + o) =
+                        make_uint2(tc::pack_bf16x2(x.x, x.y), tc::pack_bf16x2(x.z, x.w));
+                }
                 ss.x = fmaf(x.x, x.x, ss.x); ss.y = fmaf(x.y, x.y, ss.y);
                 ss.z = fmaf(x.z, x.z, ss.z); ss.w = fmaf(x.w, x.w, ss.w);
             }
@@ -1000,10 +1013,11 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
             return DION_ERR_CUDA;
         TcGemmEpi e2 = e;
         e2.M = n; e2.tiles_m = (int)cdiv(n, kBM); e2.sc = (long long)n * rp;
+        e2.Cf = R; e2.C = R16;   // R (float32) and R16 straight from the epilogue (P16's columns past r are zero)
         DION_TRY(tc_gemm<256>("dion_btp_tc", tA2, tB2, m, e2, st));
         const int nchunks = (int)cdiv(n, kRChunk);
-        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
-                        batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel<false>, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r,
+                        rp, 1, batch, (const float*)R, R, R16, normp, rcount, inv, floor_nrm, status));
     } else {
     // 2. P partials = B Q (with n % 8 == 0 the pass also stores B in bf16)
     CUtensorMap tmQt;
@@ -1035,7 +1049,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
             return DION_ERR_CUDA;
         TcGemmEpi e{};
         e.M = n; e.N = rp; e.tiles_m = (int)cdiv(n, kBM); e.tiles_n = (int)cdiv(rp, bn); e.batch = batch;
-        e.Cf = part; e.ldc = rp; e.sc = (long long)n * rp; e.alpha = 0.f; e.beta = 1.f; e.status = status;
+        e.Cf = R; e.C = R16; e.ldc = rp; e.sc = (long long)n * rp; e.alpha = 0.f; e.beta = 1.f; e.status = status;
         e.nseg = 1; e.zmul = 1;
         cudaError_t ce;
         if (bn == 64) ce = tc_gemm<64, true>("dion_btp_tc", tA, tB, m, e, st);
@@ -1043,9 +1057,9 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         else if (bn == 192) ce = tc_gemm<192, true>("dion_btp_tc", tA, tB, m, e, st);
         else ce = tc_gemm<256, true>("dion_btp_tc", tA, tB, m, e, st);
         DION_TRY(ce);
-        // 7. R = the one partial, R16, column norms, Q = R / ||R_j||, Q16
-        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp, 1,
-                        batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
+        // 7. column norms of R (the GEMM wrote R and R16; P16's columns past r are zero)
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel<false>, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r,
+                        rp, 1, batch, (const float*)R, R, R16, normp, rcount, inv, floor_nrm, status));
     } else {
         CUtensorMap tmP64;
         if (!make_tmap_3d(&tmP64, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
@@ -1056,8 +1070,8 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, false};
         DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, tmP64, pa, st));
         // 7. R = sum of partials, R16, column norms, Q = R / ||R_j||, Q16
-        DION_TRY(launch("dion_rsum", dion_rsum_kernel, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r, rp,
-                        splits, batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
+        DION_TRY(launch("dion_rsum", dion_rsum_kernel<true>, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r,
+                        rp, splits, batch, (const float*)part, R, R16, normp, rcount, inv, floor_nrm, status));
     }
     }
     {
@@ -1112,12 +1126,12 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         if (ua.kchunks <= 4) {
             static std::atomic<unsigned long long> pattr{0};
             DION_TRY(smem_attr_once((const void*)dion_update_persist_kernel<3, 2>, (int)upd_smem<3, 2>(), pattr));
-            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<3, 2>, dim3(grid), dim3(192), upd_smem<3, 2>(),
+            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<3, 2>, dim3(grid), dim3(kUpdThreads), upd_smem<3, 2>(),
                             st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
         } else {
             static std::atomic<unsigned long long> pattr_w{0};
             DION_TRY(smem_attr_once((const void*)dion_update_persist_kernel<5, 1>, (int)upd_smem<5, 1>(), pattr_w));
-            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<5, 1>, dim3(grid), dim3(192), upd_smem<5, 1>(),
+            DION_TRY(launch("dion_update_tc", dion_update_persist_kernel<5, 1>, dim3(grid), dim3(kUpdThreads), upd_smem<5, 1>(),
                             st, tmPa, tmR, tmQ, tmM, tmG, tmX, ua));
         }
     } else {
