@@ -171,10 +171,17 @@ def kernel_cost(name, w, state):
         g, r = st["g"], st["r"]
         rp = -(-r // 64) * 64
         mn = g.batch * g.m * g.n
-        if name.startswith("dion_bq"):
-            tot += mn * (4 + eb) + g.batch * (g.n * r * 2 + g.m * rp * 4)
+        # which B the products read: wide ranks (rp > 256) form bf16 B and B^T
+        # once (dion_formb); narrow bf16 ranks with n % 8 == 0 store bf16 B from
+        # the B Q pass; otherwise both passes form B from M and G
+        wide = eb == 2 and rp > 256
+        b16 = eb == 2 and not wide and g.n % 8 == 0
+        if name.startswith("dion_formb"):
+            tot += mn * (4 + eb + 2 + 2)
+        elif name.startswith("dion_bq"):
+            tot += mn * (2 if wide else (4 + eb + (2 if b16 else 0))) + g.batch * (g.n * r * 2 + g.m * rp * 4)
         elif name.startswith("dion_btp"):
-            tot += mn * (4 + eb) + g.batch * (g.m * rp * 2 + g.n * rp * 4)
+            tot += mn * (2 if (wide or b16) else (4 + eb)) + g.batch * (g.m * rp * 2 + g.n * rp * (6 if (wide or b16) else 4))
         elif name.startswith("dion_update"):
             tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * rp * 2 + 2 * g.n * rp * 2)
         elif name == "chol_inv_pass1":
