@@ -109,6 +109,12 @@ struct PassArgs {
     float* part;            // [split][batch][rows][rp] fp32 partial products
     int* status;
     bool store_b;           // B Q pass only: also store B = M + G, as rounded for the MMA, through tmS
+    // B Q pass with one split only, if P3 is set: the epilogue writes the
+    // three bf16 terms of P (term t of matrix b at P3 + (3 b + t) m rp, the
+    // first CholeskyQR pass's input) instead of the float32 partial, and P
+    // itself as float32 to Pf when set (the blocked factorization's input)
+    bf16* P3;
+    float* Pf;
 };
 
 constexpr int kProducers = 512;                  // warps 0..15 build the B tiles
@@ -251,6 +257,7 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
             const uint32_t idesc = tc::make_idesc(kBM, nN, 1, MN_A, true);
             int stage = 0, it = 0;
             uint32_t ph = 0;
+            int pend = -1;   // stage whose release waits for its B store to finish reading it
             for (int u = blockIdx.x; u < units && !*abrt; u += gridDim.x, ++it) {
                 int b, split, tile, kc0, nk;
                 unit_of(u, b, split, tile, kc0, nk);
@@ -272,19 +279,31 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
                     }
                     if (!MN_A && a.store_b) {
                         // the bf16 B tile (128 rows x 64 columns, 128-byte swizzled as the
-                        // tensor map expects) to global memory for the B^T P GEMM; the
-                        // stage is released only after the store has read it
+                        // tensor map expects) to global memory for the B^T P GEMM.  A stage
+                        // is released only after its store has read it; the store of this
+                        // chunk stays in flight and releases its stage one chunk later
                         tc::tma_store_3d(&tmS, smem + stage * kStage, (kc0 + kc) * kBK, tile * kBM, b);
                         tc::tma_store_commit();
-                        tc::tma_store_wait_read();
+                        if (pend >= 0) {
+                            tc::tma_store_wait_read1();
+                            tc::mma_commit(&empty[pend]);
+                        }
+                        pend = stage;
+                    } else {
+                        tc::mma_commit(&empty[stage]);
                     }
-                    tc::mma_commit(&empty[stage]);
                     if (++stage == kStages) { stage = 0; ph ^= 1; }
                 }
                 if (!ok) break;
                 tc::mma_commit(&acc_full[buf]);
             }
-            if (!MN_A && a.store_b) tc::tma_store_wait_all();
+            if (!MN_A && a.store_b) {
+                if (pend >= 0) {
+                    tc::tma_store_wait_read();
+                    tc::mma_commit(&empty[pend]);
+                }
+                tc::tma_store_wait_all();
+            }
         }
     } else {
         // ---------------- epilogue: TMEM -> fp32 partials
@@ -298,16 +317,56 @@ __global__ void __launch_bounds__(kPassWarps * 32, 1) dion_pass_kernel(const __g
             tc::tc_fence_after();
             const int row = tile * kBM + q * 32 + lane;
             float* out = a.part + (((long long)split * a.batch + b) * out_rows + row) * a.rp;
+            const long long pn = (long long)a.m * a.rp, po = (long long)row * a.rp;
             for (int c0 = 0; c0 < nN; c0 += 32) {
                 uint32_t v[32];
                 tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256 + c0), v);
                 tc::tmem_ld_wait();
                 if (row < out_rows) {
+                    if (!MN_A && a.P3) {
+                        // the split of P into three bf16 terms (24 significant bits), columns
+                        // past r are zero already (so are those of Q)
+                        bf16* t0 = a.P3 + 3ll * b * pn + po + c0;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(out + c0 + j) =
-                            make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                                        __uint_as_float(v[j + 3]));
+                        for (int j = 0; j < 32; j += 4) {
+                            uint32_t w[3][2];
+#pragma unroll
+                            for (int h = 0; h < 4; h += 2) {
+                                uint32_t p1 = 0, p2 = 0, p3 = 0;
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const float x = __uint_as_float(v[j + h + e]);
+                                    const bf16 h1 = __float2bfloat16_rn(x);
+                                    const float r1 = x - __bfloat162float(h1);
+                                    const bf16 h2 = __float2bfloat16_rn(r1);
+                                    const bf16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+                                    p1 |= (uint32_t)__bfloat16_as_ushort(h1) << (16 * e);
+                                    p2 |= (uint32_t)__bfloat16_as_ushort(h2) << (16 * e);
+                                    p3 |= (uint32_t)__bfloat16_as_ushort(h3) << (16 * e);
+                                }
+                                w[0][h / 2] = p1;
+                                w[1][h / 2] = p2;
+                                w[2][h / 2] = p3;
+                            }
+#pragma unroll
+                            for (int t = 0; t < 3; ++t)
+                                *reinterpret_cast<uint2*>(t0 + t * pn + j) = make_uint2(w[t][0], w[t][1]);
+                        }
+                        if (a.Pf) {
+                            float* pf = a.Pf + (long long)b * pn + po + c0;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(pf + j) =
+                                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(out + c0 + j) =
+                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                            __uint_as_float(v[j + 3]));
+                    }
                 }
             }
             tc::tc_fence_before();
@@ -1031,11 +1090,15 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int kchunks = (int)cdiv(n, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, B16 != nullptr};
+        // one split: the epilogue writes the terms of P (and, for the blocked
+        // factorization, P as float32) for the first CholeskyQR pass directly
+        const bool terms = splits == 1;
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, B16 != nullptr,
+                    terms ? (bf16*)(ws + L.P3) : nullptr, (terms && L.nbc > 0) ? P1 : nullptr};
         DION_TRY(launch_pass<false>("dion_bq_tc", vec, tmQt, tmS, pa, st));
-        // 3-5. CholeskyQR2; its first pass reads the split partials of P directly, its
-        // last product writes P (float32, P0) and P16 = bf16(P)
-        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st, n, M, G, Q));
+        // 3-5. CholeskyQR2; its first pass reads the split partials of P directly (or the
+        // terms above), its last product writes P (float32, P0) and P16 = bf16(P)
+        DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, splits, P0, P1, P16, ws, L, status, st, n, M, G, Q, terms));
     }
     // 6. R partials = B^T P
     const int nchunks = (int)cdiv(n, kRChunk);
@@ -1067,7 +1130,7 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         const int kchunks = (int)cdiv(m, kBK);
         const int kcps = (int)cdiv(kchunks, L.ksplit_r);
         const int splits = (int)cdiv(kchunks, kcps);
-        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, false};
+        PassArgs pa{m, n, rp, batch, splits, kcps, kchunks, M, G, part, status, false, nullptr, nullptr};
         DION_TRY(launch_pass<true>("dion_btp_tc", vec, tmP64, tmP64, pa, st));
         // 7. R = sum of partials, R16, column norms, Q = R / ||R_j||, Q16
         DION_TRY(launch("dion_rsum", dion_rsum_kernel<true>, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r,

@@ -94,9 +94,11 @@ int chol_block_size(int r);
 // CholeskyQR2 on the tensor cores (3-term bf16 splits, fp32 accuracy); see qr_tc.cu.
 // M, G, Q, n: the step's inputs (B = M + G is m x n), for the float64 first
 // pass of flagged matrices; Pin (the B Q partials) may be overwritten there.
+// terms_ready: the B Q pass already wrote the three bf16 terms of P to P3
+// (and, for the blocked factorization, P as float32 to Ptmp); Pin is unused.
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const struct DionLayout& L, int* status, cudaStream_t st,
-                            int n, const float* M, const bf16* G, const float* Q);
+                            int n, const float* M, const bf16* G, const float* Q, bool terms_ready = false);
 
 dion_status dion_step_simt(int batch, int m, int n, int r, dion_dtype dt, void* X, const void* G, float* M,
                            float* Q, float mu, float lr, float wd, const float* hyper, char* ws, const DionLayout& L,

@@ -437,7 +437,7 @@ int chol_block_size(int r) { return r > kCholOneCtaMaxR ? kCholBlock : 0; }
 
 cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* Pin, int nparts, float* P, float* Ptmp,
                             bf16* P16, char* ws, const DionLayout& L, int* status, cudaStream_t st, int n,
-                            const float* M, const bf16* G, const float* Q)
+                            const float* M, const bf16* G, const float* Q, bool terms_ready)
 {
     bf16* P3 = (bf16*)(ws + L.P3);
     bf16* P3b = (bf16*)(ws + L.P3b);
@@ -486,7 +486,7 @@ cudaError_t qr_cholesky2_tc(int batch, int m, int r, int rp, float* Pin, int npa
         float* dst = pass == 0 ? Ptmp : P;
         const int ti = (pass == 1 && !blocked) ? 1 : 0;   // which terms hold this pass's input
         cudaError_t e = cudaSuccess;
-        if (pass == 0) {
+        if (pass == 0 && !terms_ready) {
             const long long total4 = (long long)m * (rp / 4);
             e = launch("qr_split", qr_split_kernel, dim3((unsigned)std::min<long long>(cdiv(total4, 256), 2048), batch),
                        dim3(256), 0, st, m, r, rp, src, nparts, (long long)batch * m * rp, P3,
