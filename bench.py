@@ -177,7 +177,7 @@ def kernel_cost(name, w, state):
         wide = eb == 2 and rp > 256
         b16 = eb == 2 and not wide and g.n % 8 == 0
         if name.startswith("dion_formb"):
-            tot += mn * (4 + eb + 2 + 2)
+            tot += mn * (4 + eb + 2)
         elif name.startswith("dion_bq"):
             tot += mn * (2 if wide else (4 + eb + (2 if b16 else 0))) + g.batch * (g.n * r * 2 + g.m * rp * 4)
         elif name.startswith("dion_btp"):

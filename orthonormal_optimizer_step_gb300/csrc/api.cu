@@ -64,17 +64,14 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
         L.normp = carve(off, b * (size_t)cdiv(n, 32) * rp * f);
         L.rcount = carve(off, b * sizeof(int));
         L.emax = carve(off, b * sizeof(int));
-        if (L.wide) {
-            const size_t mp = align_up((size_t)m, 8), np = align_up((size_t)n, 8);
+        if (L.wide) {   // bf16 B, read K-major by B Q and MN-major by B^T P
+            const size_t np = align_up((size_t)n, 8);
             L.B16 = carve(off, b * m * np * h);
-            L.B16T = carve(off, b * n * mp * h);
-            L.P16T = carve(off, b * rp * mp * h);
         } else if (n % 8 == 0) {   // the B Q pass stores B = M + G in bf16 for the B^T P GEMM
             L.b16_narrow = true;
             L.B16 = carve(off, b * m * (size_t)n * h);
-            L.B16T = L.P16T = off;
         } else {
-            L.B16 = L.B16T = L.P16T = off;
+            L.B16 = off;
         }
         L.S64 = L.S6;   // 6 b r r floats hold the 2 b r r doubles of the float64 first pass
         L.nbc = chol_block_size(r);
@@ -88,7 +85,7 @@ DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt)
     } else {
         L.nbc = 0;
         L.wide = false;
-        L.ZJ = L.A3 = L.B16 = L.B16T = L.P16T = off;
+        L.ZJ = L.A3 = L.B16 = off;
         L.Ppart = L.Qt16 = L.P16 = L.R16 = L.Q16 = off;
         L.P3 = L.P3b = L.Z3 = L.S6 = L.normp = L.rcount = L.emax = off;
         L.S64 = carve(off, 2 * b * r * r * sizeof(double));

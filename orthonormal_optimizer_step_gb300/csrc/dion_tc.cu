@@ -750,95 +750,48 @@ __global__ void __launch_bounds__(256) dion_prep_qt_kernel(int n, int r, int rp,
 }
 
 // ------------------------------------------------- wide ranks (rp > 256)
-// B = M + G as bf16 once, row-major (B16, pitch pb) and transposed (B16T,
-// pitch mp), for the two TMA GEMMs that replace the fused passes when the
-// rank spans several 256-column chunks (the fused passes would re-read M and
-// G once per chunk).  64 x 64 tiles; the transpose goes through shared memory.
+// B = M + G as bf16 once, row-major (B16, pitch pb), for the two TMA GEMMs
+// that replace the fused passes when the rank spans several 256-column chunks
+// (the fused passes would re-read M and G once per chunk): B Q reads it
+// K-major, B^T P MN-major.  One thread per 16 consecutive elements of a row.
 template <bool VEC>
-__global__ void __launch_bounds__(256) dion_formb_kernel(int m, int n, long long pb, long long mp, const float* M,
-                                                         const bf16* G, bf16* B16, bf16* B16T)
+__global__ void __launch_bounds__(256) dion_formb_kernel(int m, int n, long long pb, const float* M, const bf16* G,
+                                                         bf16* B16)
 {
-    __shared__ __align__(16) bf16 tile[64][72];
     const int b = blockIdx.z, c0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
     const size_t base = (size_t)b * m * n;
-    {
-        const int ri = threadIdx.x >> 2, cg = (threadIdx.x & 3) * 16, i = i0 + ri, c = c0 + cg;
-        float v[16];
-        if (VEC && i < m && c + 16 <= n) {
-            const float* mr = M + base + (size_t)i * n + c;
-            const bf16* gr = G + base + (size_t)i * n + c;
+    const int ri = threadIdx.x >> 2, cg = (threadIdx.x & 3) * 16, i = i0 + ri, c = c0 + cg;
+    if (i >= m || c >= n) return;
+    float v[16];
+    if (VEC && c + 16 <= n) {
+        const float* mr = M + base + (size_t)i * n + c;
+        const bf16* gr = G + base + (size_t)i * n + c;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(mr + 4 * q));
-                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint4 g = __ldg(reinterpret_cast<const uint4*>(gr + 8 * q));
-                const bf16* h = reinterpret_cast<const bf16*>(&g);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[8 * q + e] += __bfloat162float(h[e]);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const size_t o = base + (size_t)i * n + c + e;
-                v[e] = (i < m && c + e < n) ? M[o] + __bfloat162float(G[o]) : 0.f;
-            }
+        for (int q = 0; q < 4; ++q) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(mr + 4 * q));
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
         }
-        uint4 w[2];
-        w[0] = make_uint4(tc::pack_bf16x2(v[0], v[1]), tc::pack_bf16x2(v[2], v[3]), tc::pack_bf16x2(v[4], v[5]),
-                          tc::pack_bf16x2(v[6], v[7]));
-        w[1] = make_uint4(tc::pack_bf16x2(v[8], v[9]), tc::pack_bf16x2(v[10], v[11]), tc::pack_bf16x2(v[12], v[13]),
-                          tc::pack_bf16x2(v[14], v[15]));
-        *reinterpret_cast<uint4*>(&tile[ri][cg]) = w[0];
-        *reinterpret_cast<uint4*>(&tile[ri][cg + 8]) = w[1];
-        if (i < m) {
-            bf16* o = B16 + (size_t)b * m * pb + (size_t)i * pb + c;
-            if (c + 16 <= n) {
-                *reinterpret_cast<uint4*>(o) = w[0];
-                *reinterpret_cast<uint4*>(o + 8) = w[1];
-            } else {
-                for (int e = 0; c + e < n && e < 16; ++e) o[e] = tile[ri][cg + e];
-            }
-        }
-    }
-    __syncthreads();
-    {
-        const int cj = threadIdx.x >> 2, rg = (threadIdx.x & 3) * 16, c = c0 + cj, i = i0 + rg;
-        if (c < n) {
-            uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w[e] = (uint32_t)__bfloat16_as_ushort(tile[rg + 2 * e][cj]) |
-                       ((uint32_t)__bfloat16_as_ushort(tile[rg + 2 * e + 1][cj]) << 16);
-            bf16* o = B16T + (size_t)b * n * mp + (size_t)c * mp + i;
-            if (i + 16 <= m) {
-                *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-                for (int e = 0; i + e < m && e < 16; ++e) o[e] = tile[rg + e][cj];
-            }
+        for (int q = 0; q < 2; ++q) {
+            const uint4 g = __ldg(reinterpret_cast<const uint4*>(gr + 8 * q));
+            const bf16* h = reinterpret_cast<const bf16*>(&g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[8 * q + e] += __bfloat162float(h[e]);
+        }
+        bf16* o = B16 + (size_t)b * m * pb + (size_t)i * pb + c;
+        *reinterpret_cast<uint4*>(o) = make_uint4(tc::pack_bf16x2(v[0], v[1]), tc::pack_bf16x2(v[2], v[3]),
+                                                  tc::pack_bf16x2(v[4], v[5]), tc::pack_bf16x2(v[6], v[7]));
+        *reinterpret_cast<uint4*>(o + 8) = make_uint4(tc::pack_bf16x2(v[8], v[9]), tc::pack_bf16x2(v[10], v[11]),
+                                                      tc::pack_bf16x2(v[12], v[13]), tc::pack_bf16x2(v[14], v[15]));
+    } else {
+        bf16* o = B16 + (size_t)b * m * pb + (size_t)i * pb;
+        for (int e = 0; e < 16 && c + e < n; ++e) {
+            const size_t x = base + (size_t)i * n + c + e;
+            o[c + e] = __float2bfloat16_rn(M[x] + __bfloat162float(G[x]));
         }
     }
 }
 
-// out[b] (cols x rows, pitch ldo) = in[b]^T (rows x cols, pitch ldi), bf16.
-__global__ void __launch_bounds__(256) dion_transpose16_kernel(int rows, int cols, long long ldi, long long si,
-                                                               long long ldo, long long so, const bf16* in, bf16* out)
-{
-    __shared__ bf16 tile[64][66];
-    const int b = blockIdx.z, c0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
-    for (int e = threadIdx.x; e < 64 * 64; e += 256) {
-        const int ri = e >> 6, cj = e & 63, i = i0 + ri, c = c0 + cj;
-        tile[ri][cj] = (i < rows && c < cols) ? in[(size_t)b * si + (size_t)i * ldi + c] : __float2bfloat16_rn(0.f);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < 64 * 64; e += 256) {
-        const int cj = e >> 6, ri = e & 63, i = i0 + ri, c = c0 + cj;
-        if (i < rows && c < cols) out[(size_t)b * so + (size_t)c * ldo + i] = tile[ri][cj];
-    }
-}
 
 // Q16 = bf16(Q) (n x rp, row-major, padding columns zero): the MN-major
 // operand of B Q (rp <= 256).  Four columns per thread.  Also zeroes the
@@ -1043,14 +996,13 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
                         dim3((unsigned)std::min<long long>(cdiv((long long)n * (rp / 4), 256), 1024), batch), dim3(256),
                         0, st, n, r, rp, (const float*)Q, Q16, rcount));
     }
-    const long long mp = (long long)align_up((size_t)m, 8);
     if (L.wide) {
         // 2'. B = M + G once in bf16 (and B^T); P = B Q as a TMA GEMM into part (one split)
         bf16* B16 = (bf16*)(ws + L.B16);
-        bf16* B16T = (bf16*)(ws + L.B16T);
+        // B in bf16, row-major only: B^T P below reads it MN-major
         auto fk = vec ? dion_formb_kernel<true> : dion_formb_kernel<false>;
         DION_TRY(launch("dion_formb", fk, dim3((unsigned)cdiv(n, 64), (unsigned)cdiv(m, 64), batch), dim3(256), 0, st, m,
-                        n, np, mp, (const float*)M, G, B16, B16T));
+                        n, np, (const float*)M, G, B16));
         CUtensorMap tA, tB;
         if (!make_tmap_3d(&tA, B16, TmapType::BF16, n, m, batch, np * 2, (long long)m * np * 2, 64, kBM) ||
             !make_tmap_3d(&tB, Qt16, TmapType::BF16, n, rp, batch, np * 2, rp * np * 2, 64, 256))
@@ -1061,19 +1013,16 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         e.nseg = 1; e.zmul = 1;
         DION_TRY(tc_gemm<256>("dion_bq_tc", tA, tB, n, e, st));
         DION_TRY(qr_cholesky2_tc(batch, m, r, rp, part, 1, P0, P1, P16, ws, L, status, st, n, M, G, Q));
-        // 6'. R = B^T P: A = B^T (n x m), B = P^T (rp x m), both K-major
-        bf16* P16T = (bf16*)(ws + L.P16T);
-        DION_TRY(launch("dion_transpose_p", dion_transpose16_kernel,
-                        dim3((unsigned)cdiv(rp, 64), (unsigned)cdiv(m, 64), batch), dim3(256), 0, st, m, rp,
-                        (long long)rp, (long long)m * rp, mp, (long long)rp * mp, (const bf16*)P16, P16T));
+        // 6'. R = B^T P: A = B^T read MN-major from the row-major bf16 B (64 x 64
+        // boxes), B operand = P16 read MN-major; no transposed copies
         CUtensorMap tA2, tB2;
-        if (!make_tmap_3d(&tA2, B16T, TmapType::BF16, m, n, batch, mp * 2, (long long)n * mp * 2, 64, kBM) ||
-            !make_tmap_3d(&tB2, P16T, TmapType::BF16, m, rp, batch, mp * 2, rp * mp * 2, 64, 256))
+        if (!make_tmap_3d(&tA2, B16, TmapType::BF16, n, m, batch, np * 2, (long long)m * np * 2, 64, 64) ||
+            !make_tmap_3d(&tB2, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, 64))
             return DION_ERR_CUDA;
         TcGemmEpi e2 = e;
         e2.M = n; e2.tiles_m = (int)cdiv(n, kBM); e2.sc = (long long)n * rp;
         e2.Cf = R; e2.C = R16;   // R (float32) and R16 straight from the epilogue (P16's columns past r are zero)
-        DION_TRY(tc_gemm<256>("dion_btp_tc", tA2, tB2, m, e2, st));
+        DION_TRY((tc_gemm<256, true>("dion_btp_tc", tA2, tB2, m, e2, st)));
         const int nchunks = (int)cdiv(n, kRChunk);
         DION_TRY(launch("dion_rsum", dion_rsum_kernel<false>, dim3((unsigned)nchunks, batch), dim3(256), 0, st, n, r,
                         rp, 1, batch, (const float*)R, R, R16, normp, rcount, inv, floor_nrm, status));

@@ -24,9 +24,9 @@ struct DionLayout {
     size_t hard;            // per matrix (batch + 1 ints): the float32 first pass found an unresolved
                             // pivot; entry batch: any matrix did
     size_t S64;             // float64 Gram and inverse factor of the fallback first pass (2 batch r r doubles)
-    bool wide;              // rp > 256: B formed once in bf16 for both products
+    bool wide;              // rp > 256: B formed once in bf16 (B16) for both products
     bool b16_narrow;        // rp <= 256, n % 8 == 0: the B Q pass stores bf16 B (B16) for a TMA B^T P
-    size_t B16, B16T, P16T; // bf16 B [m][round8(n)], B^T [n][round8(m)], P^T [rp][round8(m)]
+    size_t B16;             // bf16 B [m][round8(n)] (wide ranks), [m][n] (narrow, n % 8 == 0)
     size_t total;
 };
 DionLayout dion_layout(int batch, int m, int n, int r, dion_dtype dt);
