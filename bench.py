@@ -217,6 +217,29 @@ def kernel_cost(name, w, state):
     return bound, tot
 
 
+# Tensor-core flops of one step's launches of a streaming kernel: B Q and
+# B^T P are 2 m n r each, the update's two products 4 m n r.  At wide ranks
+# these, not the bytes, can set the kernel's floor.
+def kernel_flops(name, w, state):
+    tot = 0.0
+    for st in state:
+        g, r = st["g"], st["r"]
+        mn = g.batch * g.m * g.n
+        if name.startswith("dion_bq") or name.startswith("dion_btp"):
+            tot += 2.0 * mn * r
+        elif name.startswith("dion_update"):
+            tot += 4.0 * mn * r
+    return tot
+
+
+# The floor of a kernel that both streams bytes and runs tensor products is
+# the larger of the two times; returns (bound, cost) for that floor.
+def mixed_bound(bound, cost, flops, hbm_gbs, bf16_tflops):
+    if bound == "hbm" and flops / (bf16_tflops * 1e12) > cost / (hbm_gbs * 1e9):
+        return "tensor", flops
+    return bound, cost
+
+
 def alu_peak_tflops(sm_mhz=2070.0, sms=152):
     """fp32 FMA peak: SMs x 128 lanes x 2 flops x clock."""
     return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
@@ -340,6 +363,9 @@ def run_gb300(args, rank, world, local_rank):
         dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else (None, (0, 0.0))
         dom_name, (dom_launches, dom_ms) = dom
         bound, cost_step = kernel_cost(dom_name or "", w, state)
+        bound_bytes = bound == "hbm"
+        bound, cost_step = mixed_bound(bound, cost_step, kernel_flops(dom_name or "", w, state), pk["hbm_gbs"],
+                                       pk["bf16_tflops"])
         per_launch_ms = dom_ms / max(dom_launches, 1)
         achieved, peak, unit = None, None, None
         if bound and dom_ms > 0:
@@ -351,20 +377,26 @@ def run_gb300(args, rank, world, local_rank):
             else:
                 achieved, peak, unit = rate / 1e12, alu_peak_tflops(), "TFLOP/s"
         # every streaming kernel's own fraction, for context
-        per_kernel = {}
+        per_kernel, per_kernel_t = {}, {}
         for k, (nl, kms) in kernels.items():
             kb, kc = kernel_cost(k, w, state)
             if kb == "hbm" and kms > 0:
                 per_kernel[k] = round(kc * args.steps / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
+                kf = kernel_flops(k, w, state)
+                if mixed_bound(kb, kc, kf, pk["hbm_gbs"], pk["bf16_tflops"])[0] == "tensor":
+                    per_kernel_t[k] = round(kf * args.steps / (kms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)
         traffic, traffic_src = profiled_traffic(w.name, dom_name) if dom_name else (None, "no kernel")
         roofline = {"bound": bound or "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": unit,
                     "frac": (achieved / peak) if achieved and peak else None, "traffic": traffic,
                     "traffic_unit": "bytes per launch (dram read + write, ncu)", "traffic_source": traffic_src,
-                    "algorithmic_bytes_per_launch": cost_step / max(dom_launches / args.steps, 1) if bound == "hbm"
-                    else None,
+                    "algorithmic_bytes_per_launch": kernel_cost(dom_name, w, state)[1] / max(dom_launches / args.steps, 1)
+                    if bound_bytes else None,
                     "peak_source": pk["source"] if bound != "alu" else "derived: 152 SMs x 128 FMA x 2 x 2070 MHz",
                     "launches": dom_launches, "ms_per_launch": per_launch_ms,
                     "hbm_frac_by_kernel": per_kernel,
+                    # streaming kernels whose tensor products outweigh their
+                    # bytes (wide ranks): fraction of the bf16 peak instead
+                    "tensor_frac_by_kernel": per_kernel_t,
                     "step_hbm_floor_ms": by / (pk["hbm_gbs"] * 1e9) * 1e3,
                     "step_tensor_floor_ms": fl / (pk["bf16_tflops"] * 1e12) * 1e3,
                     "step_frac_of_floor": max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)) * 1e3

@@ -1102,6 +1102,9 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         // wide ranks: the two products as persistent 128 x 256 TMA GEMMs with
         // the updates fused into their epilogues (M and X in place):
         //   M <- M + G - (1 - mu) P R^T,   X <- (1 - lr wd) X - lr sqrt(m/n) P Q^T
+        // Eight epilogue warps with the coalesced (shared-memory transposed)
+        // epilogue: the M epilogue streams 10 bytes per element from and to
+        // HBM, more than four warps' row-per-lane accesses can cover.
         CUtensorMap tP, tRb, tQb;
         if (!make_tmap_3d(&tP, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||
             !make_tmap_3d(&tRb, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256) ||
@@ -1115,14 +1118,14 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         e1.aux2 = G; e1.ldaux2 = n; e1.saux2 = mn; e1.alpha2 = 1.f;
         e1.hp = hp; e1.hp_mode = 1; e1.status = status; e1.nseg = 1; e1.zmul = 1;
         e1.m_fast = e1.tiles_m < e1.tiles_n;
-        DION_TRY(tc_gemm<256>("dion_update_tc", tP, tRb, rp, e1, st));
+        DION_TRY((tc_gemm<256, false, 8, 1>("dion_update_tc", tP, tRb, rp, e1, st)));
         TcGemmEpi e2{};
         e2.M = m; e2.N = n; e2.tiles_m = e1.tiles_m; e2.tiles_n = e1.tiles_n; e2.batch = batch;
         e2.C = X; e2.ldc = n; e2.sc = mn;
         e2.aux = X; e2.ldaux = n; e2.saux = mn;
         e2.hp = hp; e2.hp_mode = 2; e2.status = status; e2.nseg = 1; e2.zmul = 1;
         e2.m_fast = e2.tiles_m < e2.tiles_n;
-        DION_TRY(tc_gemm<256>("dion_update_tc", tP, tQb, rp, e2, st));
+        DION_TRY((tc_gemm<256, false, 8, 2>("dion_update_tc", tP, tQb, rp, e2, st)));
     } else if (vec) {
         // persistent TMA-epilogue pass (needs 16-byte aligned rows of M, G, X)
         CUtensorMap tmM, tmG, tmX;

@@ -7,9 +7,16 @@
 // walks the output tiles (BM = 128 rows, BN = 64/128/192/256 columns) of every
 // matrix of the batch.  Warp 0 issues TMA loads into a ring of shared-memory
 // stages, warp 1 issues tcgen05.mma from one thread into a double-buffered
-// TMEM accumulator, warps 2..5 drain the accumulator (tcgen05.ld), apply the
-// epilogue and store bf16 results (optionally also the transpose), so the
-// epilogue of one tile overlaps the MMAs of the next.
+// TMEM accumulator, warps 2..2+EW-1 drain the accumulator (tcgen05.ld), apply
+// the epilogue and store the results (optionally also the transpose), so the
+// epilogue of one tile overlaps the MMAs of the next.  EW = 4 gives one warp
+// per TMEM lane quarter; EW = 8 or 12 split each quarter's columns between
+// two or three warps, for epilogues that read float32 addends from HBM and
+// need more loads in flight than four warps keep.  COAL routes each warp's
+// 32 x 32 accumulator block through a padded shared-memory tile, so that its
+// global loads and stores cover four whole 128-byte row segments per
+// instruction instead of 32 rows (one per lane): the form for epilogues that
+// stream their addends and outputs from and to HBM.
 #pragma once
 
 #include <cuda.h>
@@ -242,14 +249,140 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
     }
 }
 
+// Coalesced epilogue of one 32 x 32 block: tb holds the block (row i at
+// tb[33 i]), rows row0.. and columns col0.. of the output.  Lane l handles
+// columns col0 + 4 (l % 8) .. +3 of rows 4p + l / 8, p = 0..7, so each
+// instruction moves four whole row segments.  Supports the float32 and bf16
+// addends (auxf or aux, then aux2) and the float32 and bf16 outputs (Cf, C).
+// Interior blocks with aligned rows ("fast") load all of a lane's addends
+// into a TcCoalPref, branch-free, before any arithmetic (so their latencies
+// overlap); edge blocks go element by element.
+__device__ __forceinline__ bool tc_coal_aligned(const void* p, long long ld, long long sm, unsigned bytes)
+{
+    return p == nullptr || (((uintptr_t)p & (bytes - 1)) == 0 && (ld & 3) == 0 && (sm & 3) == 0);
+}
+
+__device__ __forceinline__ bool tc_coal_rows_aligned(const TcGemmEpi& ep)
+{
+    return tc_coal_aligned(ep.auxf, ep.ldauxf, ep.sauxf, 16) && tc_coal_aligned(ep.aux, ep.ldaux, ep.saux, 8) &&
+           tc_coal_aligned(ep.aux2, ep.ldaux2, ep.saux2, 8) && tc_coal_aligned(ep.Cf, ep.ldc, ep.sc, 16) &&
+           tc_coal_aligned(ep.C, ep.ldc, ep.sc, 8);
+}
+
+// one lane's addends of a fast block: a = auxf (float4) or aux (bf16 x 4 in
+// the first two words), a2 = aux2 (bf16 x 4)
+struct TcCoalPref {
+    float4 a[8];
+    uint2 a2[8];
+};
+
+__device__ __forceinline__ void tc_coal_prefetch(const TcGemmEpi& ep, int b, int row0, int col0, int lane,
+                                                 TcCoalPref& pf)
+{
+    const long long r = (long long)(row0 + (lane >> 3));
+    const int gc = col0 + 4 * (lane & 7);
+    if (ep.auxf) {
+        const float* ap = ep.auxf + b * ep.sauxf + r * ep.ldauxf + gc;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) pf.a[p] = *reinterpret_cast<const float4*>(ap + 4 * p * ep.ldauxf);
+    } else if (ep.aux) {
+        const bf16* ap = ep.aux + b * ep.saux + r * ep.ldaux + gc;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const uint2 u = *reinterpret_cast<const uint2*>(ap + 4 * p * ep.ldaux);
+            pf.a[p].x = __uint_as_float(u.x);
+            pf.a[p].y = __uint_as_float(u.y);
+        }
+    }
+    if (ep.aux2) {
+        const bf16* ap = ep.aux2 + b * ep.saux2 + r * ep.ldaux2 + gc;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) pf.a2[p] = *reinterpret_cast<const uint2*>(ap + 4 * p * ep.ldaux2);
+    }
+}
+
+__device__ __forceinline__ void tc_coal_add_bf16x4(float (&o)[4], uint32_t lo, uint32_t hi, float w)
+{
+    o[0] = fmaf(w, __uint_as_float(lo << 16), o[0]);
+    o[1] = fmaf(w, __uint_as_float(lo & 0xffff0000u), o[1]);
+    o[2] = fmaf(w, __uint_as_float(hi << 16), o[2]);
+    o[3] = fmaf(w, __uint_as_float(hi & 0xffff0000u), o[3]);
+}
+
+__device__ __forceinline__ void tc_coal_finish(const TcGemmEpi& ep, int b, int row0, int col0, const float* tb,
+                                               int lane, float alpha, float beta, const TcCoalPref& pf)
+{
+    const int cl = 4 * (lane & 7), r8 = lane >> 3;
+    const long long r = (long long)(row0 + r8);
+    const int gc = col0 + cl;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = beta * tb[(4 * p + r8) * 33 + cl + e];
+        if (ep.auxf) {
+            o[0] = fmaf(alpha, pf.a[p].x, o[0]);
+            o[1] = fmaf(alpha, pf.a[p].y, o[1]);
+            o[2] = fmaf(alpha, pf.a[p].z, o[2]);
+            o[3] = fmaf(alpha, pf.a[p].w, o[3]);
+        } else if (ep.aux) {
+            tc_coal_add_bf16x4(o, __float_as_uint(pf.a[p].x), __float_as_uint(pf.a[p].y), alpha);
+        }
+        if (ep.aux2) tc_coal_add_bf16x4(o, pf.a2[p].x, pf.a2[p].y, ep.alpha2);
+        const long long off = (r + 4 * p) * ep.ldc + gc;
+        if (ep.Cf) *reinterpret_cast<float4*>(ep.Cf + b * ep.sc + off) = make_float4(o[0], o[1], o[2], o[3]);
+        if (ep.C)
+            *reinterpret_cast<uint2*>(ep.C + b * ep.sc + off) =
+                make_uint2(tc::pack_bf16x2(o[0], o[1]), tc::pack_bf16x2(o[2], o[3]));
+    }
+}
+
+// this warp's 32 x 32 accumulator block (TMEM address tq: its lane quarter,
+// first column) into tb, row `lane` at tb[33 lane], 16 columns at a time
+__device__ __forceinline__ void tc_coal_stage(uint32_t tq, float* tb, int lane)
+{
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t v[16];
+        tc::tmem_ld16(tq + 16 * half, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tb[lane * 33 + 16 * half + j] = __uint_as_float(v[j]);
+    }
+    __syncwarp();
+}
+
+// edge blocks: element by element, every access guarded
+__device__ __forceinline__ void tc_coal_slow(const TcGemmEpi& ep, int b, int row0, int col0, const float* tb, int lane,
+                                             float alpha, float beta)
+{
+    const int cl = 4 * (lane & 7), r8 = lane >> 3, gc = col0 + cl;
+#pragma unroll 1
+    for (int p = 0; p < 8; ++p) {
+        const int gr = row0 + 4 * p + r8;
+#pragma unroll 1
+        for (int e = 0; e < 4; ++e) {
+            const int c = gc + e;
+            if (gr >= ep.M || c >= ep.N) continue;
+            float v = beta * tb[(4 * p + r8) * 33 + cl + e];
+            if (ep.auxf) v = fmaf(alpha, ep.auxf[b * ep.sauxf + (long long)gr * ep.ldauxf + c], v);
+            else if (ep.aux) v = fmaf(alpha, __bfloat162float(ep.aux[b * ep.saux + (long long)gr * ep.ldaux + c]), v);
+            if (ep.aux2) v = fmaf(ep.alpha2, __bfloat162float(ep.aux2[b * ep.saux2 + (long long)gr * ep.ldaux2 + c]), v);
+            if (ep.Cf) ep.Cf[b * ep.sc + (long long)gr * ep.ldc + c] = v;
+            if (ep.C) ep.C[b * ep.sc + (long long)gr * ep.ldc + c] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
 // MN = true: both operands are MN-major (the M or N index contiguous, K
 // rows): tmA and tmB have 64 x 64 boxes (MN x K) landing as 64-wide MN blocks
 // of the 128-byte swizzle (8 KB apart), so a row-major m x r panel serves as
 // the operand of its own Gram matrix without a transposed copy.
-template <int BN, bool MN = false>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, bool MN = false, int EW = 4, int COAL = 0>
+__global__ void __launch_bounds__(64 + 32 * EW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int K, TcGemmEpi ep)
 {
+    static_assert(EW % 4 == 0 && EW >= 4 && EW <= 12, "epilogue warps: 4, 8 or 12");
     using Cfg = TcGemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -269,7 +402,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&acc_full[b], 1);
-            tc::mbar_init(&acc_empty[b], 4);
+            tc::mbar_init(&acc_empty[b], EW);
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -368,6 +501,7 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;   // which of the quarter's EW / 4 column slices
         float alpha = ep.alpha, beta = ep.beta;
         if (ep.hp_mode) {
             float one_minus_mu, decay, scale;
@@ -381,6 +515,105 @@ __global__ void __launch_bounds__(192, 1)
             if (blockIdx.x == 0 && warp == 2 && lane == 0 && !ep.hp.finite()) atomicOr(ep.status, kStatusNonFinite);
         }
         int it = 0;
+        if constexpr (COAL == 2) {
+            // bf16 addend (aux) to bf16 output (C): a lane's addends for all
+            // NCH blocks of the tile (8 x 4 bf16 each) are loaded before the
+            // accumulator wait, so they arrive under the tile's MMAs
+            constexpr int STEP = 32 * (EW / 4), NCH = BN / STEP;
+            static_assert(BN % STEP == 0, "whole 32-column blocks per epilogue warp");
+            float* tb = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
+            const bool rows_aligned = tc_coal_rows_aligned(ep);
+            const int cl = 4 * (lane & 7), r8 = lane >> 3;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
+                const int b = t / per_mat, rem = t % per_mat;
+                int tm, tn;
+                tc_tile_mn(ep, rem, tm, tn);
+                if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
+                const int buf = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                ++it;
+                const int row0 = tm * Cfg::BM + q * 32, colw = tn * BN + h * 32;
+                const bool fast = rows_aligned && row0 + 32 <= ep.M && colw + (NCH - 1) * STEP + 32 <= ep.N;
+                const long long off0 = b * ep.saux + (long long)(row0 + r8) * ep.ldaux + colw + cl;
+                uint2 xs[NCH][8];
+                if (fast) {
+#pragma unroll
+                    for (int k = 0; k < NCH; ++k)
+#pragma unroll
+                        for (int p = 0; p < 8; ++p)
+                            xs[k][p] = *reinterpret_cast<const uint2*>(ep.aux + off0 + 4 * p * ep.ldaux + k * STEP);
+                }
+                if (!tc::mbar_wait(&acc_full[buf], aph, abrt, ep.status)) break;
+                tc::tc_fence_after();
+                const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 32);
+#pragma unroll
+                for (int k = 0; k < NCH; ++k) {
+                    const int col0 = colw + k * STEP;
+                    tc_coal_stage(tq + k * STEP, tb, lane);
+                    if (fast) {
+                        const long long offc = b * ep.sc + (long long)(row0 + r8) * ep.ldc + col0 + cl;
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            float o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) o[e] = beta * tb[(4 * p + r8) * 33 + cl + e];
+                            tc_coal_add_bf16x4(o, xs[k][p].x, xs[k][p].y, alpha);
+                            *reinterpret_cast<uint2*>(ep.C + offc + 4 * p * ep.ldc) =
+                                make_uint2(tc::pack_bf16x2(o[0], o[1]), tc::pack_bf16x2(o[2], o[3]));
+                        }
+                    } else if (row0 < ep.M && col0 < ep.N) {
+                        tc_coal_slow(ep, b, row0, col0, tb, lane, alpha, beta);
+                    }
+                    __syncwarp();
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+            }
+        } else if constexpr (COAL == 1) {
+            // per tile, this warp's NCH blocks of 32 x 32 (columns h * 32 +
+            // k * STEP), one after another: stage the block, load its
+            // addends (all of a lane's loads issued together), finish it.
+            // (Loading the next block's addends ahead, in a second register
+            // set, measured slower: the extra loads in flight throttled the
+            // load/store unit.)  tb: this warp's block, row `lane` at
+            // tb[33 lane] (the padding makes both the row writes and the
+            // four-rows-at-a-time reads conflict-free).
+            constexpr int STEP = 32 * (EW / 4), NCH = BN / STEP;
+            static_assert(BN % STEP == 0, "whole 32-column blocks per epilogue warp");
+            float* tb = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
+            const bool rows_aligned = tc_coal_rows_aligned(ep);
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
+                const int b = t / per_mat, rem = t % per_mat;
+                int tm, tn;
+                tc_tile_mn(ep, rem, tm, tn);
+                if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
+                const int buf = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                ++it;
+                if (!tc::mbar_wait(&acc_full[buf], aph, abrt, ep.status)) break;
+                tc::tc_fence_after();
+                const int row0 = tm * Cfg::BM + q * 32, colw = tn * BN + h * 32;
+                const bool rows_in = rows_aligned && row0 + 32 <= ep.M;
+                const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 32);
+#pragma unroll 1
+                for (int k = 0; k < NCH; ++k) {
+                    const int col0 = colw + k * STEP;
+                    tc_coal_stage(tq + k * STEP, tb, lane);
+                    if (rows_in && col0 + 32 <= ep.N) {
+                        TcCoalPref pf;
+                        tc_coal_prefetch(ep, b, row0, col0, lane, pf);
+                        tc_coal_finish(ep, b, row0, col0, tb, lane, alpha, beta, pf);
+                    } else if (row0 < ep.M && col0 < ep.N) {
+                        tc_coal_slow(ep, b, row0, col0, tb, lane, alpha, beta);
+                    }
+                    __syncwarp();
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+            }
+        } else {
         for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
             const int b = t / per_mat, rem = t % per_mat;
             int tm, tn;
@@ -393,7 +626,7 @@ __global__ void __launch_bounds__(192, 1)
             tc::tc_fence_after();
             const int row = tm * Cfg::BM + q * 32 + lane;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = h * 32; c0 < BN; c0 += 32 * (EW / 4)) {
                 uint32_t v[32];
                 tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
                 tc::tmem_ld_wait();
@@ -403,6 +636,7 @@ __global__ void __launch_bounds__(192, 1)
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+        }
         }
     }
     __syncthreads();
@@ -414,17 +648,25 @@ __global__ void __launch_bounds__(192, 1)
 
 // Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN
 // (MN: both 64 x 64, MN x K).
-template <int BN, bool MN = false>
+// COAL (1 or 2): the epilogue transposes through EW blocks of 32 x 33 floats
+// placed after the stages and barriers; it serves the addends and the
+// float32/bf16 outputs only (not Cs3 or CT).  COAL = 2 is the bf16 addend to
+// bf16 output form (aux and C only), which loads a whole tile's addends ahead.
+template <int BN, bool MN = false, int EW = 4, int COAL = 0>
 cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
                     cudaStream_t st)
 {
     using Cfg = TcGemmCfg<BN>;
+    constexpr size_t smem = Cfg::SMEM + (COAL ? (size_t)EW * 32 * 33 * 4 : 0);
+    static_assert(smem <= 232448, "shared memory per CTA");
+    if (COAL && (ep.Cs3 || ep.CT)) return cudaErrorInvalidValue;
+    if (COAL == 2 && (!ep.aux || !ep.C || ep.auxf || ep.aux2 || ep.Cf)) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> attr{0};
-    cudaError_t e = smem_attr_once((const void*)tc_gemm_kernel<BN, MN>, (int)Cfg::SMEM, attr);
+    cudaError_t e = smem_attr_once((const void*)tc_gemm_kernel<BN, MN, EW, COAL>, (int)smem, attr);
     if (e != cudaSuccess) return e;
     const int tiles = ep.batch * ep.tiles_m * ep.tiles_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    return launch(name, tc_gemm_kernel<BN, MN>, dim3(grid), dim3(192), Cfg::SMEM, st, tmA, tmB, K, ep);
+    return launch(name, tc_gemm_kernel<BN, MN, EW, COAL>, dim3(grid), dim3(64 + 32 * EW), smem, st, tmA, tmB, K, ep);
 }
 
 }  // namespace

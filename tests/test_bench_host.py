@@ -36,3 +36,17 @@ def test_profiled_traffic_reads_summary_and_checks_sources(tmp_path, monkeypatch
 def test_csrc_digest_covers_the_sources():
     d = bench.csrc_digest()
     assert len(d) == 64 and d == bench.csrc_digest()
+
+
+def test_streaming_kernel_bound_follows_the_larger_floor():
+    """At rank 1024 the update's 4 m n r flops outweigh its 14 m n bytes (so
+    its floor is the tensor one); at rank 256 the bytes set it."""
+    peaks = dict(hbm_gbs=6790.7, bf16_tflops=1919.3)
+    for w, want in ((wl.llama3_405b_layer(), "tensor"), (wl.llama3_8b(), "hbm")):
+        state = [{"g": g, "r": g.rank(w.fraction)} for g in w.groups if g.rank(w.fraction) >= 256]
+        b, c = bench.kernel_cost("dion_update_tc", w, state)
+        f = bench.kernel_flops("dion_update_tc", w, state)
+        assert b == "hbm" and c > 0 and f > 0
+        got, cost = bench.mixed_bound(b, c, f, **peaks)
+        assert got == want and cost == (f if want == "tensor" else c)
+    assert bench.mixed_bound("alu", 1.0, 1e30, **peaks) == ("alu", 1.0)
