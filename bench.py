@@ -8,7 +8,9 @@ the same way and reported under "muon".
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
 Prints one JSON line (rank 0).  Inputs are synthetic (workloads/), resident in
-HBM and larger than L2, so no L2 flush is needed between steps.  Timing: CUDA
+HBM.  Workloads whose X, G and M total less than three times the L2 size get
+an L2 flush (a 258 MB write) before every timed step, outside that step's
+event pair; larger ones need none.  Timing: CUDA
 events on the launching stream, a barrier plus torch.cuda.synchronize() on both
 sides, max over ranks.  Per-kernel device times come from libdion's event
 recording around every launch inside the timed region.  "e2e" repeats the
@@ -259,6 +261,21 @@ def max_over_ranks(ms, world, device):
     return float(t.item())
 
 
+L2_BYTES = 129 * 1000 ** 2     # GB300 L2
+
+
+def input_footprint(w):
+    """Bytes of X, G and M a step streams (bf16 or f32 X and G, f32 M)."""
+    eb = 2 if str(w.dtype).endswith("bfloat16") else 4
+    return sum(g.batch * g.m * g.n * (2 * eb + 4) for g in w.groups)
+
+
+def needs_l2_flush(w):
+    """Workloads whose inputs are not several times the L2 size get an L2
+    flush before every timed step, outside the step's own event pair."""
+    return input_footprint(w) < 3 * L2_BYTES
+
+
 def job_value(ms_per_step, world):
     """Whole-job time per megabatch: each of the world replicas steps its own
     megabatch in ms_per_step (the max over ranks), so the job advances world
@@ -314,19 +331,35 @@ def run_gb300(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # Small workloads: a 2 x L2 buffer is written before every timed step, and
+    # each step is timed by its own event pair, so that no step starts with
+    # its inputs in L2 and the flush itself is not timed.
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if needs_l2_flush(w) else None
+
     def timed(fn, steps, prof=None):
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if prof is not None:
             prof.__enter__()
-        e0.record()
-        for _ in range(steps):
-            fn()
-        e1.record()
+        if flush_buf is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                fn()
+            e1.record()
+        else:
+            pairs = []
+            for _ in range(steps):
+                flush_buf.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                pairs.append((e0, e1))
         if prof is not None:
             prof.__exit__(None, None, None)
         barrier()
-        return max_over_ranks(e0.elapsed_time(e1), world, dev)
+        ms = e0.elapsed_time(e1) if flush_buf is None else sum(a.elapsed_time(b) for a, b in pairs)
+        return max_over_ranks(ms, world, dev)
 
     clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                     if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
@@ -509,7 +542,11 @@ def run_gb300(args, rank, world, local_rank):
                 "config": {"workload": w.name, "groups": [[g.batch, g.m, g.n, g.rank(w.fraction)]
                                                           for g in w.groups],
                            "rank_fraction": w.fraction, "params": w.params,
-                           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                           "l2": (f"L2 flushed before every timed step ({2 * L2_BYTES // 10**6} MB written, "
+                                  f"outside the step's events); X, G, M {input_footprint(w) // 10**6} MB"
+                                  if needs_l2_flush(w) else
+                                  f"inputs larger than L2 (no flush): X, G, M {input_footprint(w) // 10**6} MB"),
+                           "parallelism": f"replicas x{world}",
                            "group_streams": len(state) if args.group_streams else 1},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clk, "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},

@@ -1102,9 +1102,10 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         // wide ranks: the two products as persistent 128 x 256 TMA GEMMs with
         // the updates fused into their epilogues (M and X in place):
         //   M <- M + G - (1 - mu) P R^T,   X <- (1 - lr wd) X - lr sqrt(m/n) P Q^T
-        // Eight epilogue warps with the coalesced (shared-memory transposed)
-        // epilogue: the M epilogue streams 10 bytes per element from and to
-        // HBM, more than four warps' row-per-lane accesses can cover.
+        // Coalesced (shared-memory transposed) epilogues with eight warps.
+        // The M product streams 10 bytes per element from and to HBM; the X
+        // product (4 bytes per element, bound by its MMAs) loads a whole
+        // tile's X ahead of the accumulator.
         CUtensorMap tP, tRb, tQb;
         if (!make_tmap_3d(&tP, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||
             !make_tmap_3d(&tRb, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256) ||

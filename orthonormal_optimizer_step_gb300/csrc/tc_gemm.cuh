@@ -98,6 +98,25 @@ struct TcGemmCfg {
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
 };
 
+// Operand stages of a GEMM whose epilogue stages through EW blocks of 32 x 33
+// floats (COAL != 0): as many of the configuration's stages as fit beside
+// them in the 227 KB a CTA may use.
+template <int BN, int EW, int COAL>
+constexpr int tc_stages()
+{
+    using Cfg = TcGemmCfg<BN>;
+    if (!COAL) return Cfg::STAGES;
+    const int fit = (int)((232448 - 1024 - 256 - (size_t)EW * 32 * 33 * 4) / Cfg::STAGE_BYTES);
+    return fit < Cfg::STAGES ? fit : Cfg::STAGES;
+}
+
+template <int BN, int EW, int COAL>
+constexpr size_t tc_smem()
+{
+    return (size_t)tc_stages<BN, EW, COAL>() * TcGemmCfg<BN>::STAGE_BYTES + 1024 + 256 +
+           (COAL ? (size_t)EW * 32 * 33 * 4 : 0);
+}
+
 int num_sms();
 
 // Kernels defined in this header get internal linkage: every translation unit
@@ -383,12 +402,14 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int K, TcGemmEpi ep)
 {
     static_assert(EW % 4 == 0 && EW >= 4 && EW <= 12, "epilogue warps: 4, 8 or 12");
+    constexpr int STAGES = tc_stages<BN, EW, COAL>();
+    static_assert(STAGES >= 3, "operand stages");
     using Cfg = TcGemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = (uint64_t*)(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
-    uint64_t* empty = full + Cfg::STAGES;
-    uint64_t* acc_full = empty + Cfg::STAGES;
+    uint64_t* full = (uint64_t*)(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = (uint32_t*)(acc_empty + 2);
     int* abort_flag = (int*)(tmem_slot + 1);
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Cfg::STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
@@ -452,7 +473,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
                             tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
                             tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
                         }
-                        if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                        if (++stage == STAGES) { stage = 0; ph ^= 1; }
                     }
                 }
             }
@@ -492,7 +513,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
                                          idesc, (kc | k) != 0);
                     }
                     tc::mma_commit(&empty[stage]);
-                    if (++stage == Cfg::STAGES) { stage = 0; ph ^= 1; }
+                    if (++stage == STAGES) { stage = 0; ph ^= 1; }
                 }
                 if (!ok) break;
                 tc::mma_commit(&acc_full[buf]);
@@ -521,7 +542,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
             // accumulator wait, so they arrive under the tile's MMAs
             constexpr int STEP = 32 * (EW / 4), NCH = BN / STEP;
             static_assert(BN % STEP == 0, "whole 32-column blocks per epilogue warp");
-            float* tb = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
+            float* tb = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
             const bool rows_aligned = tc_coal_rows_aligned(ep);
             const int cl = 4 * (lane & 7), r8 = lane >> 3;
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
@@ -581,7 +602,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
             // four-rows-at-a-time reads conflict-free).
             constexpr int STEP = 32 * (EW / 4), NCH = BN / STEP;
             static_assert(BN % STEP == 0, "whole 32-column blocks per epilogue warp");
-            float* tb = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
+            float* tb = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + 256) + (warp - 2) * (32 * 33);
             const bool rows_aligned = tc_coal_rows_aligned(ep);
             for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x) {
                 const int b = t / per_mat, rem = t % per_mat;
@@ -649,15 +670,16 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
 // Launches the GEMM; tmA has boxes of 64 x 128 (K x rows), tmB of 64 x BN
 // (MN: both 64 x 64, MN x K).
 // COAL (1 or 2): the epilogue transposes through EW blocks of 32 x 33 floats
-// placed after the stages and barriers; it serves the addends and the
-// float32/bf16 outputs only (not Cs3 or CT).  COAL = 2 is the bf16 addend to
-// bf16 output form (aux and C only), which loads a whole tile's addends ahead.
+// placed after the stages and barriers (tc_stages() keeps as many operand
+// stages as fit beside them); it serves the addends and the float32/bf16
+// outputs only (not Cs3 or CT).  COAL = 2 is the bf16 addend to bf16 output
+// form (aux and C only), which loads a whole tile's addends ahead.
 template <int BN, bool MN = false, int EW = 4, int COAL = 0>
 cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
                     cudaStream_t st)
 {
     using Cfg = TcGemmCfg<BN>;
-    constexpr size_t smem = Cfg::SMEM + (COAL ? (size_t)EW * 32 * 33 * 4 : 0);
+    constexpr size_t smem = tc_smem<BN, EW, COAL>();
     static_assert(smem <= 232448, "shared memory per CTA");
     if (COAL && (ep.Cs3 || ep.CT)) return cudaErrorInvalidValue;
     if (COAL == 2 && (!ep.aux || !ep.C || ep.auxf || ep.aux2 || ep.Cf)) return cudaErrorInvalidValue;

@@ -50,3 +50,10 @@ def test_streaming_kernel_bound_follows_the_larger_floor():
         got, cost = bench.mixed_bound(b, c, f, **peaks)
         assert got == want and cost == (f if want == "tensor" else c)
     assert bench.mixed_bound("alu", 1.0, 1e30, **peaks) == ("alu", 1.0)
+
+
+def test_l2_flush_only_for_workloads_near_the_l2_size():
+    assert bench.input_footprint(wl.square(1024)) == 8 * 1024 * 1024 * 8
+    assert bench.needs_l2_flush(wl.square(1024)) and bench.needs_l2_flush(wl.square(2048))
+    for w in (wl.square(4096), wl.gpt_small(), wl.llama3_8b(), wl.llama3_405b_layer()):
+        assert not bench.needs_l2_flush(w)
