@@ -186,10 +186,13 @@ def kernel_cost(name, w, state):
             tot += mn * (2 if (wide or b16) else (4 + eb)) + g.batch * (g.m * rp * 2 + g.n * rp * (6 if (wide or b16) else 4))
         elif name.startswith("dion_update"):
             tot += mn * (4 + eb + eb + 4 + eb) + g.batch * (g.m * rp * 2 + 2 * g.n * rp * 2)
-        elif name == "chol_inv_pass1":
+        elif name in ("chol_inv_pass1", "chol_inv_pass2"):
+            # Cholesky r^3/3 + triangular inverse r^3/3; the second pass is
+            # counted as a full factorization (its launches return at once for
+            # matrices whose Gram passed the near-identity test)
             bound = "alu"
             if r <= 248:
-                tot += g.batch * (2.0 / 3.0) * r ** 3      # Cholesky r^3/3 + triangular inverse r^3/3
+                tot += g.batch * (2.0 / 3.0) * r ** 3
         elif name == "qr_gram_tc" or name == "qr_apply_tc":
             bound = "tensor"
             tot += g.batch * 6 * 2.0 * g.m * r * r          # six bf16 cross-term products

@@ -729,6 +729,216 @@ __global__ void __launch_bounds__(kUpdThreads, 1) dion_update_persist_kernel(
     }
 }
 
+// ------------------------------- wide-rank M update (256 < rp <= 512)
+// M <- M + G - (1 - mu) P R^T over 128 x 128 tiles of M with K = rp, as a
+// persistent kernel.  The P and R chunks stream through four 32 KB operand
+// stages.  M and G move by TMA in 32-column blocks through a ring of four
+// 24 KB slots that a warp of its own keeps loaded, so about three blocks of
+// M and G (72 KB) are in flight per SM without holding registers; each
+// block's result overwrites its M in shared memory and is stored by TMA.
+//   warp 0: operand producer   warp 1: MMA issuer   warp 2: M/G block loader
+//   warps 3..10: epilogue (warp w: TMEM lane quarter w % 4, 16-column half
+//   (w - 3) / 4 of each block)
+constexpr int kMwBN = 128, kMwOps = 4, kMwSlots = 4, kMwEpiWarps = 8;
+constexpr int kMwEpiWarp0 = 3;
+constexpr int kMwThreads = (kMwEpiWarp0 + kMwEpiWarps) * 32;
+constexpr int kMwBlocks = kMwBN / 32;                              // 32-column blocks per tile
+constexpr uint32_t kMwA = kBM * kBK * 2;                           // 16 KB P chunk
+constexpr uint32_t kMwStage = kMwA + kMwBN * kBK * 2;              // + 16 KB R chunk
+constexpr uint32_t kMwM = kBM * 32 * 4, kMwG = kBM * 32 * 2;       // 16 KB of M, 8 KB of G per block
+constexpr uint32_t kMwSlot = kMwM + kMwG;
+constexpr size_t kMwSmem = (size_t)kMwOps * kMwStage + (size_t)kMwSlots * kMwSlot + 1024 + 256;
+static_assert(kMwSmem <= 232448, "shared memory per CTA");
+static_assert(kMwSlot % 1024 == 0 && kMwM % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
+
+struct MwArgs {
+    int m, n, batch, kchunks, tiles_m, tiles_n;
+    StepHyper hp;
+    int* status;
+    int m_fast;   // row tiles fastest (see UpdPArgs)
+};
+
+// byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a box of
+// 64-byte rows stored with the 64-byte swizzle
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk)
+{
+    return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+}
+
+__global__ void __launch_bounds__(kMwThreads, 1) dion_update_mwide_kernel(
+    const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmR,
+    const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmG, MwArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* ops = smem;                                  // [kMwOps][kMwStage]
+    uint8_t* slots = smem + kMwOps * kMwStage;            // [kMwSlots][kMwSlot]
+    uint64_t* ofull = (uint64_t*)(slots + kMwSlots * kMwSlot);
+    uint64_t* oempty = ofull + kMwOps;
+    uint64_t* efull = oempty + kMwOps;
+    uint64_t* eempty = efull + kMwSlots;
+    uint64_t* afull = eempty + kMwSlots;
+    uint64_t* aempty = afull + 2;
+    uint32_t* tmem_slot = (uint32_t*)(aempty + 2);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    volatile int* abrt = abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float one_minus_mu, decay, scale;
+    a.hp.get(one_minus_mu, decay, scale);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && !a.hp.finite()) atomicOr(a.status, kStatusNonFinite);
+    const int per_mat = a.tiles_m * a.tiles_n, tiles = a.batch * per_mat;
+    auto tile_of = [&](int t, int& b, int& m0, int& n0) {
+        b = t / per_mat;
+        const int rem = t % per_mat;
+        m0 = (a.m_fast ? rem % a.tiles_m : rem / a.tiles_n) * kBM;
+        n0 = (a.m_fast ? rem / a.tiles_m : rem % a.tiles_n) * kMwBN;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMwOps; ++s) {
+            tc::mbar_init(&ofull[s], 1);
+            tc::mbar_init(&oempty[s], 1);
+        }
+        for (int s = 0; s < kMwSlots; ++s) {
+            tc::mbar_init(&efull[s], 1);
+            tc::mbar_init(&eempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&afull[s], 1);
+            tc::mbar_init(&aempty[s], kMwEpiWarps);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 2 * kMwBN);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok && !*abrt; t += gridDim.x) {
+                int b, m0, n0;
+                tile_of(t, b, m0, n0);
+                for (int kc = 0; kc < a.kchunks; ++kc) {
+                    if (!tc::mbar_wait(&oempty[stage], ph ^ 1, abrt, a.status)) { ok = false; break; }
+                    uint8_t* o = ops + stage * kMwStage;
+                    tc::mbar_arrive_expect_tx(&ofull[stage], kMwStage);
+                    tc::tma_load_3d(o, &tmP, &ofull[stage], kc * kBK, m0, b);
+                    tc::tma_load_3d(o + kMwA, &tmR, &ofull[stage], kc * kBK, n0, b);
+                    if (++stage == kMwOps) { stage = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::make_idesc(kBM, kMwBN, 1, false, false);
+            int stage = 0, it = 0;
+            uint32_t ph = 0;
+            for (int t = blockIdx.x; t < tiles && !*abrt; t += gridDim.x, ++it) {
+                const int ab = it & 1;
+                if (!tc::mbar_wait(&aempty[ab], ((it >> 1) & 1) ^ 1, abrt, a.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + ab * kMwBN;
+                bool ok = true;
+                for (int kc = 0; kc < a.kchunks; ++kc) {
+                    if (!tc::mbar_wait(&ofull[stage], ph, abrt, a.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(ops + stage * kMwStage), r0 = a0 + kMwA;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc::mma_bf16(d, tc::make_sdesc(a0 + k * 32, 16, 1024), tc::make_sdesc(r0 + k * 32, 16, 1024),
+                                     idesc, (kc | k) != 0);
+                    tc::mma_commit(&oempty[stage]);
+                    if (++stage == kMwOps) { stage = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(&afull[ab]);
+            }
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            int g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok && !*abrt; t += gridDim.x) {
+                int b, m0, n0;
+                tile_of(t, b, m0, n0);
+                for (int blk = 0; blk < kMwBlocks; ++blk, ++g) {
+                    const int s = g % kMwSlots;
+                    if (!tc::mbar_wait(&eempty[s], ((g / kMwSlots) & 1) ^ 1, abrt, a.status)) { ok = false; break; }
+                    uint8_t* e = slots + s * kMwSlot;
+                    tc::mbar_arrive_expect_tx(&efull[s], kMwSlot);
+                    tc::tma_load_3d(e, &tmM, &efull[s], n0 + 32 * blk, m0, b);
+                    tc::tma_load_3d(e + kMwM, &tmG, &efull[s], n0 + 32 * blk, m0, b);
+                }
+            }
+        }
+    } else {
+        // The trip counts here do not depend on the abort flag (every wait
+        // returns at once after an abort), so all epilogue warps pass the
+        // same named barriers.
+        const int quarter = warp & 3, h = (warp - kMwEpiWarp0) >> 2;
+        const uint32_t row = quarter * 32 + lane;     // tile row == TMEM lane
+        const bool leader = threadIdx.x == kMwEpiWarp0 * 32;
+        int it = 0, g = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+            int b, m0, n0;
+            tile_of(t, b, m0, n0);
+            const int ab = it & 1;
+            bool ok = tc::mbar_wait(&afull[ab], (it >> 1) & 1, abrt, a.status);
+            tc::tc_fence_after();
+            for (int blk = 0; blk < kMwBlocks; ++blk, ++g) {
+                const int s = g % kMwSlots;
+                ok = tc::mbar_wait(&efull[s], (g / kMwSlots) & 1, abrt, a.status) && ok;
+                uint8_t* e = slots + s * kMwSlot;
+                uint32_t pr[16];
+                tc::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kMwBN + blk * 32 + h * 16), pr);
+                tc::tmem_ld_wait();
+                if (ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {   // columns h * 16 + 4c .. + 3 of the block
+                        float4* pm = reinterpret_cast<float4*>(e + tc::sw128_offset(row, h * 4 + c));
+                        const bf16* gh =
+                            reinterpret_cast<const bf16*>(e + kMwM + sw64_offset(row, h * 2 + (c >> 1))) + (c & 1) * 4;
+                        float4 mv = *pm;
+                        mv.x = mv.x + __bfloat162float(gh[0]) - one_minus_mu * __uint_as_float(pr[4 * c + 0]);
+                        mv.y = mv.y + __bfloat162float(gh[1]) - one_minus_mu * __uint_as_float(pr[4 * c + 1]);
+                        mv.z = mv.z + __bfloat162float(gh[2]) - one_minus_mu * __uint_as_float(pr[4 * c + 2]);
+                        mv.w = mv.w + __bfloat162float(gh[3]) - one_minus_mu * __uint_as_float(pr[4 * c + 3]);
+                        *pm = mv;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(1, kMwEpiWarps * 32);
+                if (leader) {
+                    if (ok) {
+                        tc::tma_store_3d(&tmM, e, n0 + 32 * blk, m0, b);
+                        tc::tma_store_commit();
+                        tc::tma_store_wait_read();
+                    }
+                    tc::mbar_arrive(&eempty[s]);
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&aempty[ab]);
+        }
+        if (leader) tc::tma_store_wait_all();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 2 * kMwBN);
+    }
+}
+
 // ------------------------------------------------------------ small kernels
 
 // Qt[b][j][k] = bf16(Q[b][k][j]) for j < r; zero rows r <= j < rp.
@@ -1099,29 +1309,51 @@ dion_status dion_step_tc(int batch, int m, int n, int r, void* Xv, const void* G
         !make_tmap_3d(&tmQ, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, kUBN))
         return DION_ERR_CUDA;
     if (vec && L.wide) {
-        // wide ranks: the two products as persistent 128 x 256 TMA GEMMs with
-        // the updates fused into their epilogues (M and X in place):
-        //   M <- M + G - (1 - mu) P R^T,   X <- (1 - lr wd) X - lr sqrt(m/n) P Q^T
-        // Coalesced (shared-memory transposed) epilogues with eight warps.
-        // The M product streams 10 bytes per element from and to HBM; the X
-        // product (4 bytes per element, bound by its MMAs) loads a whole
-        // tile's X ahead of the accumulator.
-        CUtensorMap tP, tRb, tQb;
+        // wide ranks: the two products as persistent kernels with the updates
+        // in their epilogues (M and X in place):
+        //   M <- M + G - (1 - mu) P R^T
+        //     rp <= 512: dion_update_mwide_kernel (128 x 128 tiles; M and G move
+        //       by TMA through a ring of 32-column blocks)
+        //     rp > 512: 128 x 256 TMA GEMM with the coalesced epilogue.  There
+        //       the P and R reads from L2 (2 rp (1/128 + 1/BN) bytes per element)
+        //       outweigh the 10 bytes of M and G, and the wider tile reads fewer
+        //   X <- (1 - lr wd) X - lr sqrt(m/n) P Q^T   128 x 256 TMA GEMM with the
+        //     coalesced epilogue, a whole tile's X loaded ahead (bound by its MMAs)
+        const long long mn = (long long)m * n;
+        CUtensorMap tP, tQb;
         if (!make_tmap_3d(&tP, P16, TmapType::BF16, rp, m, batch, (long long)rp * 2, (long long)m * rp * 2, 64, kBM) ||
-            !make_tmap_3d(&tRb, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256) ||
             !make_tmap_3d(&tQb, Q16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256))
             return DION_ERR_CUDA;
-        const long long mn = (long long)m * n;
-        TcGemmEpi e1{};
-        e1.M = m; e1.N = n; e1.tiles_m = (int)cdiv(m, kBM); e1.tiles_n = (int)cdiv(n, 256); e1.batch = batch;
-        e1.Cf = M; e1.ldc = n; e1.sc = mn;
-        e1.auxf = M; e1.ldauxf = n; e1.sauxf = mn; e1.alpha = 1.f;
-        e1.aux2 = G; e1.ldaux2 = n; e1.saux2 = mn; e1.alpha2 = 1.f;
-        e1.hp = hp; e1.hp_mode = 1; e1.status = status; e1.nseg = 1; e1.zmul = 1;
-        e1.m_fast = e1.tiles_m < e1.tiles_n;
-        DION_TRY((tc_gemm<256, false, 8, 1>("dion_update_tc", tP, tRb, rp, e1, st)));
+        if (rp > 512) {
+            CUtensorMap tRb;
+            if (!make_tmap_3d(&tRb, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64, 256))
+                return DION_ERR_CUDA;
+            TcGemmEpi e1{};
+            e1.M = m; e1.N = n; e1.tiles_m = (int)cdiv(m, kBM); e1.tiles_n = (int)cdiv(n, 256); e1.batch = batch;
+            e1.Cf = M; e1.ldc = n; e1.sc = mn;
+            e1.auxf = M; e1.ldauxf = n; e1.sauxf = mn; e1.alpha = 1.f;
+            e1.aux2 = G; e1.ldaux2 = n; e1.saux2 = mn; e1.alpha2 = 1.f;
+            e1.hp = hp; e1.hp_mode = 1; e1.status = status; e1.nseg = 1; e1.zmul = 1;
+            e1.m_fast = e1.tiles_m < e1.tiles_n;
+            DION_TRY((tc_gemm<256, false, 8, 1>("dion_update_tc", tP, tRb, rp, e1, st)));
+        } else {
+            CUtensorMap tR128, tMb, tGb;
+            if (!make_tmap_3d(&tR128, R16, TmapType::BF16, rp, n, batch, (long long)rp * 2, (long long)n * rp * 2, 64,
+                              kMwBN) ||
+                !make_tmap_3d(&tMb, M, TmapType::F32, n, m, batch, (long long)n * 4, mn * 4, 32, kBM) ||
+                !make_tmap_3d_sw64(&tGb, G, TmapType::BF16, n, m, batch, (long long)n * 2, mn * 2, 32, kBM))
+                return DION_ERR_CUDA;
+            const int tm = (int)cdiv(m, kBM), tn = (int)cdiv(n, kMwBN);
+            const long long tiles = (long long)tm * tn * batch;
+            const int grid = (int)std::min<long long>(tiles, num_sms());
+            MwArgs ma{m, n, batch, (int)cdiv(rp, kBK), tm, tn, hp, status, tm < tn ? 1 : 0};
+            static std::atomic<unsigned long long> mattr{0};
+            DION_TRY(smem_attr_once((const void*)dion_update_mwide_kernel, (int)kMwSmem, mattr));
+            DION_TRY(launch("dion_update_tc", dion_update_mwide_kernel, dim3(grid), dim3(kMwThreads), kMwSmem, st,
+                            tP, tR128, tMb, tGb, ma));
+        }
         TcGemmEpi e2{};
-        e2.M = m; e2.N = n; e2.tiles_m = e1.tiles_m; e2.tiles_n = e1.tiles_n; e2.batch = batch;
+        e2.M = m; e2.N = n; e2.tiles_m = (int)cdiv(m, kBM); e2.tiles_n = (int)cdiv(n, 256); e2.batch = batch;
         e2.C = X; e2.ldc = n; e2.sc = mn;
         e2.aux = X; e2.ldaux = n; e2.saux = mn;
         e2.hp = hp; e2.hp_mode = 2; e2.status = status; e2.nseg = 1; e2.zmul = 1;

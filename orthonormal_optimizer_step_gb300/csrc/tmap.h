@@ -16,4 +16,11 @@ enum class TmapType { BF16, F32 };
 bool make_tmap_3d(CUtensorMap* out, const void* base, TmapType type, uint64_t inner, uint64_t rows, uint64_t batch,
                   uint64_t row_pitch_bytes, uint64_t batch_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// The same with the 64-byte swizzle (box_inner * element size at most 64
+// bytes): 16-byte chunk c of box row r lands at r * rowbytes + 16 (c ^ ((r / 2) % 4))
+// for 64-byte rows.
+bool make_tmap_3d_sw64(CUtensorMap* out, const void* base, TmapType type, uint64_t inner, uint64_t rows,
+                       uint64_t batch, uint64_t row_pitch_bytes, uint64_t batch_pitch_bytes, uint32_t box_inner,
+                       uint32_t box_rows);
+
 }  // namespace dion
