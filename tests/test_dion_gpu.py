@@ -50,6 +50,7 @@ RAGGED = [
     (1, 1024, 1024, 288, torch.bfloat16),  # r > 256: two 256-column chunks of the rank
     (2, 700, 600, 300, torch.bfloat16),    # blocked factorization: blocks of 128, 128, 44
     (1, 1100, 1300, 520, torch.bfloat16),  # blocked factorization: four blocks and a ragged 8
+    (1, 700, 1000, 600, torch.bfloat16),   # rp > 512: the M update as a 128 x 256 GEMM, ragged edge blocks
     (1, 8, 520, 3, torch.bfloat16),        # very wide
     (2, 520, 8, 8, torch.float32),         # very tall, full rank
 ]
