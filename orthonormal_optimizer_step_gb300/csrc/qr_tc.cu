@@ -294,13 +294,18 @@ cudaError_t gemm_mn(int bn, const char* name, const CUtensorMap& ta, const CUten
     return tc_gemm<256, true>(name, ta, tb, K, ep, st);
 }
 
+// Both operands K-major: the applies, the blocked factorization's panel,
+// trailing update and solve.  Their K ranges are short (a 128-column block,
+// or rp), so the epilogue (float32, bf16 and three-term outputs, 12 bytes per
+// element for an apply) is a large part of each tile: eight epilogue warps
+// with the coalesced (shared-memory transposed) epilogue.
 cudaError_t gemm_any(int bn, const char* name, const CUtensorMap& ta, const CUtensorMap& tb, int K, const TcGemmEpi& ep,
                      cudaStream_t st)
 {
-    if (bn == 64) return tc_gemm<64>(name, ta, tb, K, ep, st);
-    if (bn == 128) return tc_gemm<128>(name, ta, tb, K, ep, st);
-    if (bn == 192) return tc_gemm<192>(name, ta, tb, K, ep, st);
-    return tc_gemm<256>(name, ta, tb, K, ep, st);
+    if (bn == 64) return tc_gemm<64, false, 8, 1>(name, ta, tb, K, ep, st);
+    if (bn == 128) return tc_gemm<128, false, 8, 1>(name, ta, tb, K, ep, st);
+    if (bn == 192) return tc_gemm<192, false, 8, 1>(name, ta, tb, K, ep, st);
+    return tc_gemm<256, false, 8, 1>(name, ta, tb, K, ep, st);
 }
 
 bool tmap_bf16(CUtensorMap* t, const bf16* base, long long inner, long long rows, long long nz, long long ld,

@@ -272,7 +272,8 @@ __device__ __forceinline__ void tc_epi_store(const TcGemmEpi& ep, int b, int row
 // tb[33 i]), rows row0.. and columns col0.. of the output.  Lane l handles
 // columns col0 + 4 (l % 8) .. +3 of rows 4p + l / 8, p = 0..7, so each
 // instruction moves four whole row segments.  Supports the float32 and bf16
-// addends (auxf or aux, then aux2) and the float32 and bf16 outputs (Cf, C).
+// addends (auxf or aux, then aux2) and the float32, bf16 and three-term bf16
+// outputs (Cf, C, Cs3).
 // Interior blocks with aligned rows ("fast") load all of a lane's addends
 // into a TcCoalPref, branch-free, before any arithmetic (so their latencies
 // overlap); edge blocks go element by element.
@@ -285,7 +286,7 @@ __device__ __forceinline__ bool tc_coal_rows_aligned(const TcGemmEpi& ep)
 {
     return tc_coal_aligned(ep.auxf, ep.ldauxf, ep.sauxf, 16) && tc_coal_aligned(ep.aux, ep.ldaux, ep.saux, 8) &&
            tc_coal_aligned(ep.aux2, ep.ldaux2, ep.saux2, 8) && tc_coal_aligned(ep.Cf, ep.ldc, ep.sc, 16) &&
-           tc_coal_aligned(ep.C, ep.ldc, ep.sc, 8);
+           tc_coal_aligned(ep.C, ep.ldc, ep.sc, 8) && tc_coal_aligned(ep.Cs3, ep.ldcs3, ep.scs3, 8);
 }
 
 // one lane's addends of a fast block: a = auxf (float4) or aux (bf16 x 4 in
@@ -353,6 +354,30 @@ __device__ __forceinline__ void tc_coal_finish(const TcGemmEpi& ep, int b, int r
         if (ep.C)
             *reinterpret_cast<uint2*>(ep.C + b * ep.sc + off) =
                 make_uint2(tc::pack_bf16x2(o[0], o[1]), tc::pack_bf16x2(o[2], o[3]));
+        if (ep.Cs3) {   // the three bf16 terms of each value (term t at + t scs3)
+            uint32_t w[3][2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t p1 = 0, p2 = 0, p3 = 0;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float x = o[2 * hh + e];
+                    const bf16 h1 = __float2bfloat16_rn(x);
+                    const float r1 = x - __bfloat162float(h1);
+                    const bf16 h2 = __float2bfloat16_rn(r1);
+                    const bf16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+                    p1 |= (uint32_t)__bfloat16_as_ushort(h1) << (16 * e);
+                    p2 |= (uint32_t)__bfloat16_as_ushort(h2) << (16 * e);
+                    p3 |= (uint32_t)__bfloat16_as_ushort(h3) << (16 * e);
+                }
+                w[0][hh] = p1;
+                w[1][hh] = p2;
+                w[2][hh] = p3;
+            }
+            bf16* sp = ep.Cs3 + 3ll * b * ep.scs3 + (r + 4 * p) * ep.ldcs3 + gc;
+#pragma unroll
+            for (int t = 0; t < 3; ++t) *reinterpret_cast<uint2*>(sp + t * ep.scs3) = make_uint2(w[t][0], w[t][1]);
+        }
     }
 }
 
@@ -389,6 +414,15 @@ __device__ __forceinline__ void tc_coal_slow(const TcGemmEpi& ep, int b, int row
             if (ep.aux2) v = fmaf(ep.alpha2, __bfloat162float(ep.aux2[b * ep.saux2 + (long long)gr * ep.ldaux2 + c]), v);
             if (ep.Cf) ep.Cf[b * ep.sc + (long long)gr * ep.ldc + c] = v;
             if (ep.C) ep.C[b * ep.sc + (long long)gr * ep.ldc + c] = __float2bfloat16_rn(v);
+            if (ep.Cs3) {
+                bf16* sp = ep.Cs3 + 3ll * b * ep.scs3 + (long long)gr * ep.ldcs3 + c;
+                const bf16 h1 = __float2bfloat16_rn(v);
+                const float r1 = v - __bfloat162float(h1);
+                const bf16 h2 = __float2bfloat16_rn(r1);
+                sp[0] = h1;
+                sp[ep.scs3] = h2;
+                sp[2 * ep.scs3] = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+            }
         }
     }
 }
@@ -671,8 +705,8 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
 // (MN: both 64 x 64, MN x K).
 // COAL (1 or 2): the epilogue transposes through EW blocks of 32 x 33 floats
 // placed after the stages and barriers (tc_stages() keeps as many operand
-// stages as fit beside them); it serves the addends and the float32/bf16
-// outputs only (not Cs3 or CT).  COAL = 2 is the bf16 addend to bf16 output
+// stages as fit beside them); it serves the addends and the float32, bf16
+// and three-term outputs (not CT).  COAL = 2 is the bf16 addend to bf16 output
 // form (aux and C only), which loads a whole tile's addends ahead.
 template <int BN, bool MN = false, int EW = 4, int COAL = 0>
 cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap& tmB, int K, const TcGemmEpi& ep,
@@ -681,8 +715,8 @@ cudaError_t tc_gemm(const char* name, const CUtensorMap& tmA, const CUtensorMap&
     using Cfg = TcGemmCfg<BN>;
     constexpr size_t smem = tc_smem<BN, EW, COAL>();
     static_assert(smem <= 232448, "shared memory per CTA");
-    if (COAL && (ep.Cs3 || ep.CT)) return cudaErrorInvalidValue;
-    if (COAL == 2 && (!ep.aux || !ep.C || ep.auxf || ep.aux2 || ep.Cf)) return cudaErrorInvalidValue;
+    if (COAL && ep.CT) return cudaErrorInvalidValue;
+    if (COAL == 2 && (!ep.aux || !ep.C || ep.auxf || ep.aux2 || ep.Cf || ep.Cs3)) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> attr{0};
     cudaError_t e = smem_attr_once((const void*)tc_gemm_kernel<BN, MN, EW, COAL>, (int)smem, attr);
     if (e != cudaSuccess) return e;
