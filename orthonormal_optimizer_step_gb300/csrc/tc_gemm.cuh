@@ -38,8 +38,10 @@ struct TcGemmEpi {
                                     // set, receives a bf16 copy
     // K segments: the contraction runs over nseg segments of K each; segment q
     // reads operand matrices zmul*b + asel[q] (A) and zmul*b + bsel[q] (B),
-    // 4-bit entries packed in asel/bsel.  seg_batch = 1: each segment is its own
-    // output matrix (index nseg*b + q) instead of being accumulated.
+    // 4-bit entries packed in asel/bsel; with K-major operands walked chunk by
+    // chunk (every segment's chunk kc before chunk kc + 1), with MN-major ones
+    // segment by segment.  seg_batch = 1: each segment is its own output
+    // matrix (index nseg*b + q) instead of being accumulated.
     int nseg, zmul, seg_batch;
     uint32_t asel, bsel;
     // float32 addend (used instead of aux when set): C = alpha * auxf + beta * acc
@@ -487,28 +489,42 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
                 if (!tc_tile_on(ep, b, tm, tn, Cfg::BM, BN)) continue;
                 const int q0 = ep.seg_batch ? b % ep.nseg : 0, q1 = ep.seg_batch ? q0 + 1 : ep.nseg;
                 const int bm = ep.seg_batch ? b / ep.nseg : b;
-                for (int q = q0; q < q1; ++q) {
+                // One stage: operand chunk kc of segment q.  K-major operands
+                // walk the segments chunk-major (for each K chunk, every
+                // segment in turn), so the operand chunks that several
+                // segments share (the split terms) are reused from L2 within a
+                // few stages instead of being fetched again per segment.
+                // MN-major operands (the Grams) walk them segment-major, so
+                // consecutive stages read consecutive rows of one term.
+                auto issue = [&](int q, int kc) -> bool {
                     const int za = bm * ep.zmul + (int)((ep.asel >> (4 * q)) & 15u);
                     const int zb = bm * ep.zmul + (int)((ep.bsel >> (4 * q)) & 15u);
-                    for (int kc = 0; kc < kchunks; ++kc) {
-                        if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) break;
-                        uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
-                        tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                        if (MN) {
+                    if (!tc::mbar_wait(&empty[stage], ph ^ 1, abrt, ep.status)) return false;
+                    uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+                    tc::mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    if (MN) {
 #pragma unroll
-                            for (int blk = 0; blk < Cfg::BM / 64; ++blk)
-                                tc::tma_load_3d(sa + blk * 8192, &tmA, &full[stage], tm * Cfg::BM + blk * 64,
-                                                kc * Cfg::BK, za);
+                        for (int blk = 0; blk < Cfg::BM / 64; ++blk)
+                            tc::tma_load_3d(sa + blk * 8192, &tmA, &full[stage], tm * Cfg::BM + blk * 64,
+                                            kc * Cfg::BK, za);
 #pragma unroll
-                            for (int blk = 0; blk < BN / 64; ++blk)
-                                tc::tma_load_3d(sa + Cfg::A_BYTES + blk * 8192, &tmB, &full[stage], tn * BN + blk * 64,
-                                                kc * Cfg::BK, zb);
-                        } else {
-                            tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
-                            tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
-                        }
-                        if (++stage == STAGES) { stage = 0; ph ^= 1; }
+                        for (int blk = 0; blk < BN / 64; ++blk)
+                            tc::tma_load_3d(sa + Cfg::A_BYTES + blk * 8192, &tmB, &full[stage], tn * BN + blk * 64,
+                                            kc * Cfg::BK, zb);
+                    } else {
+                        tc::tma_load_3d(sa, &tmA, &full[stage], kc * Cfg::BK, tm * Cfg::BM, za);
+                        tc::tma_load_3d(sa + Cfg::A_BYTES, &tmB, &full[stage], kc * Cfg::BK, tn * BN, zb);
                     }
+                    if (++stage == STAGES) { stage = 0; ph ^= 1; }
+                    return true;
+                };
+                bool ok = true;
+                if (MN) {
+                    for (int q = q0; q < q1 && ok; ++q)
+                        for (int kc = 0; kc < kchunks && ok; ++kc) ok = issue(q, kc);
+                } else {
+                    for (int kc = 0; kc < kchunks && ok; ++kc)
+                        for (int q = q0; q < q1 && ok; ++q) ok = issue(q, kc);
                 }
             }
         }
