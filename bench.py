@@ -194,8 +194,12 @@ def kernel_cost(name, w, state):
             if r <= 248:
                 tot += g.batch * (2.0 / 3.0) * r ** 3
         elif name == "qr_gram_tc" or name == "qr_apply_tc":
+            # six bf16 cross-term products per launch; both CholeskyQR passes
+            # form a Gram, and both apply through this GEMM up to rank 248
+            # (above it the first pass applies inside the blocked factorization)
             bound = "tensor"
-            tot += g.batch * 6 * 2.0 * g.m * r * r          # six bf16 cross-term products
+            per_step = 2 if (name == "qr_gram_tc" or r <= 248) else 1
+            tot += per_step * g.batch * 6 * 2.0 * g.m * r * r
         elif name == "qr_gram_sum":
             tot += g.batch * (6 * 4 + 4) * r * r            # six fp32 partials in, one out
         elif name.startswith("chol_blk_"):

@@ -57,3 +57,18 @@ def test_l2_flush_only_for_workloads_near_the_l2_size():
     assert bench.needs_l2_flush(wl.square(1024)) and bench.needs_l2_flush(wl.square(2048))
     for w in (wl.square(4096), wl.gpt_small(), wl.llama3_8b(), wl.llama3_405b_layer()):
         assert not bench.needs_l2_flush(w)
+
+
+def test_qr_product_cost_counts_every_launch_of_a_step():
+    """Two Grams per step (both CholeskyQR passes); two applies through the
+    GEMM at rank <= 248, one above (the blocked path applies the first pass)."""
+    one = lambda g, r: g.batch * 6 * 2.0 * g.m * r * r
+    w = wl.gpt_small()
+    st = [{"g": g, "r": g.rank(w.fraction)} for g in w.groups]
+    assert bench.kernel_cost("qr_gram_tc", w, st)[1] == sum(2 * one(x["g"], x["r"]) for x in st)
+    assert bench.kernel_cost("qr_apply_tc", w, st)[1] == sum(2 * one(x["g"], x["r"]) for x in st)
+    w = wl.square(16384)
+    st = [{"g": g, "r": g.rank(w.fraction)} for g in w.groups]
+    assert st[0]["r"] == 4096
+    assert bench.kernel_cost("qr_gram_tc", w, st)[1] == 2 * one(st[0]["g"], 4096)
+    assert bench.kernel_cost("qr_apply_tc", w, st)[1] == one(st[0]["g"], 4096)
